@@ -1,0 +1,132 @@
+"""fp64 CPU oracle for the fused attention forward.  TEST INFRASTRUCTURE ONLY.
+
+Only the tests, the smoke check and the CPU-baseline leg of the benchmark may
+import this module.  The product path (the CUDA library and its Python binding)
+never calls it; it shares no code, table or helper with the CUDA kernels.
+
+What it computes is the plain definition of scaled dot-product attention,
+written out step by step as an unfused pipeline:
+
+  * scores S = scale * Q K^T, materialised in full (page "Multi-Head Attention
+    的计算本质与性能瓶颈", §1, the three-op bmm / softmax / bmm example, and §2.1,
+    the Attention(Q,K,V) = softmax(QK^T/sqrt(d_k)) V decomposition);
+  * causal mask: key j is visible to query i only when j <= i, indices counted
+    from the start of each sequence (same page, §3.1, the conditional
+    assignment in the fused-kernel sketch);
+  * packed variable-length batches: sequence b owns query rows
+    cu_seqlens_q[b]:cu_seqlens_q[b+1] and key rows cu_seqlens_k[b]:cu_seqlens_k[b+1]
+    and never sees another sequence (page "长文本处理性能断层真相", §1, the
+    varlen call with int32 cu_seqlens);
+  * a full-row softmax (row max, exp, sum, divide), then P V;
+  * the per-row logsumexp LSE_i = max_j s_ij + ln sum_j exp(s_ij - max_j s_ij),
+    natural log, over the scaled and masked scores.
+
+It deliberately does NOT use the online (running max / running sum) form that
+the GPU path uses (page "深度学习算子优化：从TFLOPS幻觉到FlashAttention实战", §3),
+so the two share no algebra beyond the definition.
+
+Readings where the pages are silent:
+  * a row with no visible key (only possible for an empty key sequence) gives
+    O = 0 and LSE = -inf;
+  * causal alignment is top-left (the literal i >= j test), so it also holds
+    when a sequence has Sq != Sk.
+
+Parity status: every function here is pinned by tests/test_oracle.py (brute
+force, closed forms, invariants, a library routine); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import numpy as np
+
+
+def _as_f64(x) -> np.ndarray:
+    """Exact conversion of an fp16/bf16/fp32 torch tensor or numpy array to fp64."""
+    if hasattr(x, "detach"):  # torch tensor; bf16 has no numpy dtype, fp64 is exact
+        import torch
+        return x.detach().to(device="cpu", dtype=torch.float64).numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def attention_one_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
+                       causal: bool, rows: Optional[Sequence[int]] = None,
+                       return_p: bool = False):
+    """Attention for one (sequence, head).
+
+    q [Sq, D], k [Sk, D], v [Sk, Dv] in fp64.  ``rows`` restricts the output to
+    those query indices (indices within the sequence).  Returns (O [R, Dv],
+    LSE [R]) and, when ``return_p``, the probability matrix P [R, Sk].
+    """
+    Sq = q.shape[0]
+    Sk = k.shape[0]
+    row_idx = np.arange(Sq) if rows is None else np.asarray(rows, dtype=np.int64)
+    qs = q[row_idx]
+    # step 1: all scores, materialised
+    s = scale * (qs @ k.T)                                   # [R, Sk]
+    # step 2: mask -> visible[i, j]
+    visible = np.ones(s.shape, dtype=bool)
+    if causal:
+        visible &= np.arange(Sk)[None, :] <= row_idx[:, None]
+    s_masked = np.where(visible, s, -np.inf)
+    # step 3: full-row softmax
+    has_key = visible.any(axis=1)
+    m = np.where(has_key, s_masked.max(axis=1, initial=-np.inf), 0.0)
+    e = np.where(visible, np.exp(s_masked - m[:, None]), 0.0)
+    z = e.sum(axis=1)
+    p = np.where(has_key[:, None], e / np.where(has_key, z, 1.0)[:, None], 0.0)
+    # step 4: P V and the logsumexp
+    o = p @ v
+    with np.errstate(divide="ignore"):
+        lse = np.where(has_key, m + np.log(np.where(has_key, z, 1.0)), -np.inf)
+    if return_p:
+        return o, lse, p
+    return o, lse
+
+
+def attention_dense(q, k, v, scale: float, causal: bool,
+                    heads: Optional[Sequence[int]] = None,
+                    rows: Optional[Sequence[int]] = None):
+    """Dense batch: q [B,Sq,H,D], k/v [B,Sk,H,D] -> O [B,Sq,H,D], LSE [B,H,Sq].
+
+    With ``heads``/``rows`` only those heads/query rows are computed; the others
+    are returned as NaN so that they cannot be mistaken for checked values.
+    """
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    B, Sq, H, D = q.shape
+    Dv = v.shape[3]
+    o = np.full((B, Sq, H, Dv), np.nan)
+    lse = np.full((B, H, Sq), np.nan)
+    row_sel = np.arange(Sq) if rows is None else np.asarray(rows, dtype=np.int64)
+    for b in range(B):
+        for h in (range(H) if heads is None else heads):
+            ob, lb = attention_one_head(q[b, :, h, :], k[b, :, h, :], v[b, :, h, :],
+                                        scale, causal, rows=row_sel)
+            o[b, row_sel, h, :] = ob
+            lse[b, h, row_sel] = lb
+    return o, lse
+
+
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool,
+                     heads: Optional[Sequence[int]] = None):
+    """Packed varlen batch: q [Tq,H,D], k/v [Tk,H,D] -> O [Tq,H,D], LSE [H,Tq].
+
+    Rows of q that belong to no sequence are returned as NaN.
+    """
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    cq = [int(x) for x in np.asarray(cu_seqlens_q).tolist()]
+    ck = [int(x) for x in np.asarray(cu_seqlens_k).tolist()]
+    Tq, H, D = q.shape
+    Dv = v.shape[2]
+    o = np.full((Tq, H, Dv), np.nan)
+    lse = np.full((H, Tq), np.nan)
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if q1 == q0:
+            continue
+        for h in (range(H) if heads is None else heads):
+            ob, lb = attention_one_head(q[q0:q1, h, :], k[k0:k1, h, :], v[k0:k1, h, :],
+                                        scale, causal)
+            o[q0:q1, h, :] = ob
+            lse[h, q0:q1] = lb
+    return o, lse
