@@ -1,0 +1,407 @@
+"""Benchmark of the fused attention forward on GB300.
+
+One step = one fused forward (O and LSE) over the long-context causal workload
+B=1, H=32, Sq=Sk=65536, D=128, bf16 (inputs 1.5 GiB, larger than the 129 MB
+L2, so no flush is needed between steps).  Throughput is TFLOP/s with the
+FLOP count 4*B*H*Sq*Sk*D, halved for causal.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   (the fp64 CPU oracle on a bounded sample)
+
+Under torchrun each rank runs an independent replica on its own GPU (the
+forward has no cross-GPU exchange); the time is the max over ranks and the
+value counts the work of all ranks.  Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from scaled_dot_product_tcgen05_gb300 import workloads as W  # noqa: E402
+
+DEFAULT_WORKLOAD = "long64k_causal"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attn_fwd_kernel_long64k_causal.md")
+FALLBACK_PEAK_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------------------- ranks
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(backend: str):
+    ws, rank, _ = dist_env()
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+    return ws, rank
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a host scalar over all ranks (identity when not distributed)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def _gpu_id(self):
+        try:
+            u = torch.cuda.get_device_properties(self.dev).uuid
+            s = str(u)
+            return s if s.startswith("GPU-") else "GPU-" + s
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            if vis:
+                return vis.split(",")[self.dev]
+            return str(self.dev)
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self._gpu_id(), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[2], parts[3:7]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, _, r in rows for i in range(4) if r[i] == "Active"})
+        sm = sorted(r[0] for r in rows)
+        loaded = [r for r in sm if r > 0.5 * rows[0][1]] or sm
+        return {"sm_mhz": loaded[len(loaded) // 2], "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    return FALLBACK_PEAK_TFLOPS, "fallback (1.9 PFLOP/s bf16, earlier GB300 measurement)"
+
+
+def source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "scaled_dot_product_tcgen05_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it matches the sources."""
+    if not os.path.exists(PROFILE_SUMMARY) or workload != DEFAULT_WORKLOAD:
+        return None
+    text = open(PROFILE_SUMMARY).read()
+    m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    if not (m_t and m_h) or m_h.group(1) != source_digest():
+        return None
+    return float(m_t.group(1))
+
+
+def workload_info(wl):
+    if wl.varlen:
+        lens = W.varlen_lengths(wl).tolist()
+        flops = W.varlen_flops(lens, wl.H, wl.D, wl.causal)
+        tokens = sum(lens)
+    else:
+        flops = W.attention_flops(wl.B, wl.H, wl.Sq, wl.Sk, wl.D, wl.causal)
+        tokens = wl.B * wl.Sq
+    elem = 2
+    # algorithmic bytes: read Q, K, V once, write O (16-bit) and LSE (fp32)
+    nbytes = tokens * wl.H * wl.D * elem * 4 + tokens * wl.H * 4
+    cfg = {"workload": wl.name, "B": wl.B, "H": wl.H, "Sq": wl.Sq if not wl.varlen else tokens,
+           "Sk": wl.Sk if not wl.varlen else tokens, "D": wl.D, "causal": wl.causal,
+           "dtype": wl.dtype, "varlen": wl.varlen, "flops_per_step": flops,
+           "algorithmic_bytes_per_step": nbytes}
+    return flops, nbytes, cfg
+
+
+# ------------------------------------------------------------------ reference (oracle)
+def run_reference(args, wl, flops_full, cfg):
+    """Times the fp64 CPU oracle, as it stands, on a bounded sample of the workload."""
+    import numpy as np
+    from oracle.sdpa_oracle import attention_one_head
+
+    heads = list(range(min(2, wl.H)))
+    S = wl.Sq
+    n_rows = min(S, args.ref_rows)
+    rows = sorted(set(np.linspace(0, S - 1, n_rows).astype(np.int64).tolist()))
+    inp = W.make_inputs(wl, heads=heads) if not wl.varlen else W.make_inputs(wl)
+    q = inp["q"][0] if not wl.varlen else inp["q"]
+    k = inp["k"][0] if not wl.varlen else inp["k"]
+    v = inp["v"][0] if not wl.varlen else inp["v"]
+    qf = {h: q[:, h].double().numpy() for h in heads}
+    kf = {h: k[:, h].double().numpy() for h in heads}
+    vf = {h: v[:, h].double().numpy() for h in heads}
+    sample_flops = 0.0
+    for h in heads:
+        for i in rows:
+            keys = (i + 1) if wl.causal else wl.Sk
+            sample_flops += 4.0 * keys * wl.D
+    times = []
+    for _ in range(args.warmup):
+        attention_one_head(qf[heads[0]], kf[heads[0]], vf[heads[0]], wl.scale, wl.causal,
+                           rows=rows[: max(1, len(rows) // 8)])
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        for h in heads:
+            attention_one_head(qf[h], kf[h], vf[h], wl.scale, wl.causal, rows=rows)
+        times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    value = sample_flops / t / 1e12
+    cores = cpu_threads()
+    sample = (f"{len(heads)} heads x {len(rows)} evenly spaced query rows of {wl.name} "
+              f"(flops = 4*D*visible keys per row, {sample_flops:.3g} per step)")
+    return {"metric": "attention fwd TFLOP/s", "value": value, "unit": "TFLOP/s",
+            "impl": "reference", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": cfg,
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline_sample(wl, budget_s: float):
+    """The oracle on a bounded sample of the same workload (rank 0 only)."""
+    import numpy as np
+    from oracle.sdpa_oracle import attention_one_head
+
+    inp = W.make_inputs(wl, heads=[0]) if not wl.varlen else None
+    if inp is None:
+        return None
+    q, k, v = (inp[n][0, :, 0].double().numpy() for n in ("q", "k", "v"))
+    S = wl.Sq
+    done_flops, spent, n = 0.0, 0.0, 0
+    chunk = 64
+    rows_all = np.random.default_rng(7).permutation(S)
+    t_start = time.perf_counter()
+    while spent < budget_s and n < S:
+        rows = sorted(rows_all[n:n + chunk].tolist())
+        t0 = time.perf_counter()
+        attention_one_head(q, k, v, wl.scale, wl.causal, rows=rows)
+        spent += time.perf_counter() - t0
+        done_flops += sum(4.0 * ((i + 1) if wl.causal else wl.Sk) * wl.D for i in rows)
+        n += chunk
+    return {"value": done_flops / spent / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
+            "kind": "oracle",
+            "sample": f"{n} random query rows of head 0 of {wl.name}, "
+                      f"{time.perf_counter() - t_start:.1f} s of fp64 numpy work"}
+
+
+# ----------------------------------------------------------------------------- main
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--ref-rows", type=int, default=192)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    wl = W.standard_workloads()[args.workload]
+    flops, nbytes, cfg = workload_info(wl)
+    ws, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        cfg = dict(cfg, parallelism="replicas only (oracle on rank 0)")
+        print(json.dumps(run_reference(args, wl, flops, cfg)), flush=True)
+        return 0
+
+    import scaled_dot_product_tcgen05_gb300 as pkg
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ws, rank = init_dist("nccl")
+    pkg.load_library()
+
+    inp = W.make_inputs(wl, pin=True)
+    q_h, k_h, v_h = inp["q"], inp["k"], inp["v"]
+    cu_h = inp["cu_seqlens_q"]
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        q, k, v = (t.to(dev, non_blocking=True) for t in (q_h, k_h, v_h))
+        cu = cu_h.to(dev) if cu_h is not None else None
+        o = torch.empty_like(q)
+        lse_shape = (wl.H, q.shape[0]) if wl.varlen else (wl.B, wl.H, wl.Sq)
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+
+    def step():
+        pkg.attn_fwd(q, k, v, causal=wl.causal, scale=wl.scale, cu_seqlens_q=cu,
+                     cu_seqlens_k=cu, out=o, lse=lse, stream=stream)
+
+    # ---- kernel-only timed region (inputs resident in HBM)
+    for _ in range(args.warmup):
+        step()
+    st = pkg.attn_check(stream)
+    if st != pkg.ATTN_OK:
+        raise SystemExit(f"device status {pkg.status_string(st)}")
+    grid, smem = pkg.last_launch()
+    sampler = ClockSampler(local)
+    sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    st = pkg.attn_check(stream)
+    if st != pkg.ATTN_OK:
+        raise SystemExit(f"device status {pkg.status_string(st)}")
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = ev[0][0].elapsed_time(ev[-1][1])
+    ms_step = max_over_ranks(total_ms / args.steps, dev)
+    kernel_ms = sum(launch_ms) / len(launch_ms)
+
+    # ---- end to end through the public API, host buffers, copies inside the region
+    o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            q.copy_(q_h, non_blocking=True)
+            k.copy_(k_h, non_blocking=True)
+            v.copy_(v_h, non_blocking=True)
+            step()
+            o_h.copy_(o, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    e_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    barrier()
+    torch.cuda.synchronize()
+    e_ev[0].record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_ev[1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(e_ev[0].elapsed_time(e_ev[1]) / args.steps, dev)
+    if not (torch.isfinite(o_h.float()).all() and torch.isfinite(lse_h).all()):
+        raise SystemExit("non-finite output")
+    h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * q_h.element_size()
+    d2h = o_h.numel() * o_h.element_size() + lse_h.numel() * 4
+
+    if rank != 0:
+        return 0
+    peak, peak_src = peaks()
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    traffic = profiled_traffic(wl.name)
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample(wl, args.cpu_budget_s)
+    cfg = dict(cfg, parallelism=f"replicas x{ws}" if ws > 1 else "single GPU",
+               l2="no flush: inputs %.2f GiB > 129 MB L2" % (h2d / 2 ** 30),
+               grid_ctas=grid, smem_bytes=smem)
+    out = {
+        "metric": "attention fwd TFLOP/s", "value": flops * ws / (ms_step * 1e-3) / 1e12,
+        "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "fp16",
+        "data": "synthetic", "config": cfg,
+        "pct_of_peak": achieved / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
+                     "kernel": "attn_fwd_kernel", "kernel_ms": kernel_ms},
+        "e2e": {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

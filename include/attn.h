@@ -1,0 +1,114 @@
+/*
+ * Fused multi-head scaled-dot-product attention forward for GB300 (sm_103a).
+ *
+ *   O = softmax(scale * Q K^T + mask) V,   LSE_i = ln sum_j exp(scale * q_i . k_j)
+ *
+ * Definition: page "Multi-Head Attention的计算本质与性能瓶颈" (mlqm.cn), §1 and
+ * §2.1 (Attention(Q,K,V) = softmax(QK^T / sqrt(d_k)) V); causal rule from §3.1 of
+ * the same page (score kept when key index j <= query index i, else -inf).
+ * Packed variable-length batches follow the varlen call of page
+ * "长文本处理性能断层真相" (lnrk.cn), §1 (int32 cu_seqlens prefix offsets).
+ * The kernel tiles over key blocks with the online softmax of page
+ * "深度学习算子优化：从TFLOPS幻觉到FlashAttention实战" (jianying88.com), §3, so
+ * the Sq x Sk score matrix never reaches global memory.
+ *
+ * All functions are plain C.  Device pointers are owned by the caller; the
+ * library never frees or keeps them past the call.  Every launch is
+ * asynchronous on the caller's stream.  There is no CPU fallback: on anything
+ * other than an sm_103 device the call returns ATTN_ERR_UNSUPPORTED.
+ */
+#ifndef ATTN_TCGEN05_H
+#define ATTN_TCGEN05_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  Zero is success; every failure is negative. */
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = -1,    /* null pointer, negative size, non-finite scale, ... */
+  ATTN_ERR_UNSUPPORTED = -2,    /* head dim, dtype or device not supported */
+  ATTN_ERR_MISALIGNED = -3,     /* q/k/v/o not 16-byte aligned, lse/cu_seqlens not 4-byte */
+  ATTN_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed */
+  ATTN_ERR_DEVICE_TIMEOUT = -5, /* a kernel pipeline wait ran past its limit (reported by attn_check) */
+  ATTN_ERR_BAD_SEQLENS = -6     /* cu_seqlens not non-decreasing within [0, total] (attn_check) */
+} attn_status;
+
+typedef enum { ATTN_DTYPE_FP16 = 0, ATTN_DTYPE_BF16 = 1 } attn_dtype;
+
+/*
+ * attn_fwd -- fused attention forward (O and LSE) in one persistent kernel.
+ *
+ * Layouts (all row-major, contiguous, head dim innermost):
+ *   dense  (cu_seqlens_q == cu_seqlens_k == NULL):
+ *     q, o : [B, Sq, H, D]   k, v : [B, Sk, H, D]   lse : float [B, H, Sq]
+ *   varlen (both cu_seqlens non-NULL, int32 device arrays of B+1 entries):
+ *     q, o : [Sq, H, D]      k, v : [Sk, H, D]      lse : float [H, Sq]
+ *     Sq / Sk are the TOTAL packed rows (the allocation lengths).  Sequence b
+ *     owns query rows [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key rows
+ *     [cu_seqlens_k[b], cu_seqlens_k[b+1]); it never attends to another one.
+ *
+ * Arguments:
+ *   q, k, v   fp16 or bf16 (per dtype), 16-byte aligned device pointers.
+ *   o         output, same dtype, 16-byte aligned; written for valid rows only.
+ *   lse       output, fp32, natural-log logsumexp of the scaled, masked scores;
+ *             -inf for a row that sees no key (an empty key sequence).
+ *   B, H      batch (dense) or number of sequences (varlen); heads.  B >= 0, H >= 1.
+ *   Sq, Sk    see above.  Sk >= 1.  B == 0 or Sq == 0 is a no-op.
+ *   D         head dim, 64 or 128 (else ATTN_ERR_UNSUPPORTED).
+ *   scale     finite score scale (1/sqrt(D) is the usual choice; 0 allowed).
+ *   causal    non-zero: key j visible to query i (indices within the
+ *             sequence) only when j <= i (top-left aligned; Sq != Sk allowed).
+ *   dtype     attn_dtype.
+ *   stream    cudaStream_t (passed as void*), NULL = legacy default stream.
+ *
+ * Errors: argument, alignment, dtype and device errors are returned before
+ * anything is launched and leave o/lse untouched.  Launch failures return
+ * ATTN_ERR_CUDA.  Problems found on the device (a bad cu_seqlens array, a
+ * pipeline wait past its limit) set a per-device error word that attn_check
+ * reports; outputs of that call are then undefined.
+ * Thread-safe; per-device state is created on first use.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H, int Sq, int Sk, int D, float scale, int causal,
+             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+             int dtype, void* stream);
+
+/*
+ * attn_check -- synchronise `stream`, then report and clear the device error
+ * word of the current device: ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT,
+ * ATTN_ERR_BAD_SEQLENS, or ATTN_ERR_CUDA if the stream itself failed.
+ */
+int attn_check(void* stream);
+
+/* attn_status_string -- static, human-readable name of a status code. */
+const char* attn_status_string(int status);
+
+/*
+ * attn_num_sms -- SM count the persistent grid is sized from on the current
+ * device (>0), or a negative status.
+ */
+int attn_num_sms(void);
+
+/*
+ * attn_last_launch -- grid size (CTAs) and dynamic shared memory bytes of the
+ * most recent attn_fwd launch on this thread; either pointer may be NULL.
+ * Returns ATTN_OK, or ATTN_ERR_INVALID_ARG if nothing was launched yet.
+ */
+int attn_last_launch(int* grid_ctas, int* smem_bytes);
+
+/*
+ * attn_release -- free the library-owned per-device state (the error word) of
+ * every device it was created on.  Call only when no attn_fwd launch is in
+ * flight.  Later calls recreate the state.
+ */
+int attn_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_TCGEN05_H */

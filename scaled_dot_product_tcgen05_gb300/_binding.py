@@ -1,0 +1,179 @@
+"""ctypes binding of the C ABI in include/attn.h (argument marshalling only).
+
+Every step of the attention forward runs in the CUDA library; this module only
+checks shapes and dtypes, allocates outputs with torch, and passes raw device
+pointers and the current CUDA stream.  If the library is missing the calls
+raise: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+from .build_lib import LIB_PATH
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_MISALIGNED = -3
+ATTN_ERR_CUDA = -4
+ATTN_ERR_DEVICE_TIMEOUT = -5
+ATTN_ERR_BAD_SEQLENS = -6
+
+DTYPE_CODES = {torch.float16: 0, torch.bfloat16: 1}
+
+EXPORTED = ("attn_fwd", "attn_check", "attn_status_string", "attn_num_sms",
+            "attn_last_launch", "attn_release")
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class AttnError(RuntimeError):
+    """A non-zero status returned by the CUDA library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load (once) and return the CUDA library; raises if it was never built."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"CUDA library {p} not built; run __graft_entry__.build() "
+                               "(there is no CPU fallback)")
+        lib = ctypes.CDLL(p)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, i, vp]
+        lib.attn_fwd.restype = i
+        lib.attn_check.argtypes = [vp]
+        lib.attn_check.restype = i
+        lib.attn_status_string.argtypes = [i]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_num_sms.argtypes = []
+        lib.attn_num_sms.restype = i
+        lib.attn_last_launch.argtypes = [ctypes.POINTER(i), ctypes.POINTER(i)]
+        lib.attn_last_launch.restype = i
+        lib.attn_release.argtypes = []
+        lib.attn_release.restype = i
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().attn_status_string(int(status)).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def attn_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int,
+                 Sq: int, Sk: int, D: int, scale: float, causal: bool, cu_q_ptr: int,
+                 cu_k_ptr: int, dtype_code: int, stream: int) -> int:
+    """Direct call of the C entry point with integer device pointers; returns the status."""
+    return load_library().attn_fwd(q_ptr or None, k_ptr or None, v_ptr or None, o_ptr or None,
+                                   lse_ptr or None, B, H, Sq, Sk, D, ctypes.c_float(scale),
+                                   1 if causal else 0, cu_q_ptr or None, cu_k_ptr or None,
+                                   dtype_code, stream or None)
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = False,
+             scale: Optional[float] = None, cu_seqlens_q: Optional[torch.Tensor] = None,
+             cu_seqlens_k: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+             lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Fused attention forward on the GPU.  Returns (O, LSE).
+
+    dense : q [B,Sq,H,D], k/v [B,Sk,H,D] -> O like q, LSE fp32 [B,H,Sq]
+    varlen: q [Tq,H,D], k/v [Tk,H,D], int32 cu_seqlens [B+1] -> O like q, LSE [H,Tq]
+    ``scale`` defaults to 1/sqrt(D).  ``causal`` keeps key j for query i iff j <= i
+    (indices inside each sequence).  The launch is asynchronous on ``stream``
+    (default: torch's current stream); device-side errors are reported by
+    :func:`attn_check`.
+    """
+    varlen = cu_seqlens_q is not None or cu_seqlens_k is not None
+    if varlen and (cu_seqlens_q is None or cu_seqlens_k is None):
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must be given together")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype not in DTYPE_CODES:
+            raise ValueError(f"{name} must be fp16 or bf16, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share one dtype")
+    if varlen:
+        if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+            raise ValueError("varlen q/k/v must be [total, H, D]")
+        Tq, H, D = q.shape
+        Tk = k.shape[0]
+        if k.shape != (Tk, H, D) or v.shape != (Tk, H, D):
+            raise ValueError("k/v shape mismatch")
+        for name, c in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+            if c.dtype != torch.int32 or not c.is_cuda or c.dim() != 1 or not c.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous int32 CUDA vector")
+        if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 1:
+            raise ValueError("cu_seqlens_q/k must both have B+1 entries")
+        B, Sq, Sk = cu_seqlens_q.numel() - 1, Tq, Tk
+        lse_shape = (H, Tq)
+    else:
+        if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+            raise ValueError("dense q/k/v must be [B, S, H, D]")
+        B, Sq, H, D = q.shape
+        Sk = k.shape[1]
+        if k.shape != (B, Sk, H, D) or v.shape != (B, Sk, H, D):
+            raise ValueError("k/v shape mismatch")
+        lse_shape = (B, H, Sq)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must match q")
+    if lse is None:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    elif tuple(lse.shape) != lse_shape or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError(f"lse must be a contiguous fp32 tensor of shape {lse_shape}")
+    with torch.cuda.device(q.device):
+        st = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr(), B, H, Sq, Sk, D, float(scale), causal,
+                          cu_seqlens_q.data_ptr() if varlen else 0,
+                          cu_seqlens_k.data_ptr() if varlen else 0, DTYPE_CODES[q.dtype],
+                          _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd")
+    return out, lse
+
+
+def attn_check(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return load_library().attn_check(_stream_handle(stream))
+
+
+def num_sms() -> int:
+    return load_library().attn_num_sms()
+
+
+def last_launch() -> Tuple[int, int]:
+    g, s = ctypes.c_int(0), ctypes.c_int(0)
+    st = load_library().attn_last_launch(ctypes.byref(g), ctypes.byref(s))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_last_launch")
+    return g.value, s.value

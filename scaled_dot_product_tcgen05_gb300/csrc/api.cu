@@ -1,0 +1,275 @@
+// C ABI of the fused attention forward (declarations and contract in attn.h).
+//
+// Host side only: argument checks, per-device state (SM count, device error
+// word), TMA tensor-map encoding and the launch of the persistent kernel on the
+// caller's stream.  No synchronisation happens inside attn_fwd.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "attn.h"
+#include "fwd_kernel.cuh"
+
+namespace attn {
+
+// Instantiated in fwd_d{64,128}_{f16,bf16}.cu
+extern template cudaError_t launch_fwd<64, false>(const FwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_fwd<64, true>(const FwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_fwd<128, false>(const FwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_fwd<128, true>(const FwdParams&, int, cudaStream_t);
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  bool supported = false;
+  int sms = 0;
+  int* err = nullptr;  // device error word
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+thread_local int t_last_grid = -1;
+thread_local int t_last_smem = -1;
+
+long long timeout_ns_from_env() {
+  const char* s = std::getenv("ATTN_WAIT_TIMEOUT_MS");
+  long long ms = s ? std::atoll(s) : 0;
+  if (ms <= 0) ms = 5000;
+  return ms * 1000000LL;
+}
+
+// Creates the per-device state on first use.  Returns ATTN_OK or an error.
+int device_state(int dev, DeviceState** out) {
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    s.supported = (major == 10 && minor == 3);
+    s.sms = sms;
+    if (s.supported) {
+      if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+          return ATTN_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      }
+      if (cudaMalloc(&s.err, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+      if (cudaMemset(s.err, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    }
+    s.ready = true;
+  }
+  if (!s.supported) return ATTN_ERR_UNSUPPORTED;
+  *out = &s;
+  return ATTN_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The pointer must be device (or managed) memory reachable from `dev`.
+bool on_device(const void* p, int dev) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type == cudaMemoryTypeManaged) return true;
+  return a.type == cudaMemoryTypeDevice && a.device == dev;
+}
+
+// [rows, H, D] 16-bit tensor, box = 128 rows x 1 head x 64 elements (128 B),
+// 128-byte swizzle, zero fill outside the tensor.
+int encode_rows_heads_dim(CUtensorMap* m, const void* ptr, long long rows, int H, int D,
+                          bool bf16) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                           static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBM)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int Sq, int Sk, int D, float scale, int causal,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int dtype,
+                        void* stream) {
+  // ---- argument checks (no CUDA call before these pass)
+  if (B < 0 || H < 1 || Sq < 0 || Sk < 1) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (dtype != ATTN_DTYPE_FP16 && dtype != ATTN_DTYPE_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  const bool varlen = cu_seqlens_q != nullptr || cu_seqlens_k != nullptr;
+  if (varlen && (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || Sq == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return ATTN_ERR_MISALIGNED;
+  if (varlen && (!aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4))) return ATTN_ERR_MISALIGNED;
+  const long long rows_q = varlen ? Sq : static_cast<long long>(B) * Sq;
+  const long long rows_k = varlen ? Sk : static_cast<long long>(B) * Sk;
+  if (rows_q > INT_MAX - 2 * kUnitRows || rows_k > INT_MAX - 2 * kBN) return ATTN_ERR_INVALID_ARG;
+  // unit indices are int: B*H*ceil(Sq/256) (dense) or H*(ceil(Sq/256)+B) (varlen)
+  const long long units_bound = varlen
+      ? static_cast<long long>(H) * ((rows_q + kUnitRows - 1) / kUnitRows + B)
+      : static_cast<long long>(B) * H * ((Sq + kUnitRows - 1) / kUnitRows);
+  if (units_bound > INT_MAX / 2) return ATTN_ERR_INVALID_ARG;
+
+  // ---- device checks
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  DeviceState* ds = nullptr;
+  int st = device_state(dev, &ds);
+  if (st != ATTN_OK) return st;
+  if (!on_device(q, dev) || !on_device(k, dev) || !on_device(v, dev) || !on_device(o, dev) ||
+      !on_device(lse, dev))
+    return ATTN_ERR_INVALID_ARG;
+  if (varlen && (!on_device(cu_seqlens_q, dev) || !on_device(cu_seqlens_k, dev)))
+    return ATTN_ERR_INVALID_ARG;
+
+  // ---- parameters
+  FwdParams p;
+  const bool bf16 = dtype == ATTN_DTYPE_BF16;
+  if (encode_rows_heads_dim(&p.tm_q, q, rows_q, H, D, bf16) != ATTN_OK ||
+      encode_rows_heads_dim(&p.tm_k, k, rows_k, H, D, bf16) != ATTN_OK ||
+      encode_rows_heads_dim(&p.tm_v, v, rows_k, H, D, bf16) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+  p.o = o;
+  p.lse = lse;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.err = ds->err;
+  p.B = B;
+  p.H = H;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.varlen = varlen ? 1 : 0;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.scale_pos = scale > 0.0f ? 1 : 0;
+  p.timeout_ns = timeout_ns_from_env();
+
+  const long long grid = units_bound < ds->sms ? units_bound : ds->sms;
+  if (grid <= 0) return ATTN_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  int smem;
+  if (D == 64) {
+    smem = Layout<64>::kAlloc;
+    e = bf16 ? launch_fwd<64, true>(p, static_cast<int>(grid), s)
+             : launch_fwd<64, false>(p, static_cast<int>(grid), s);
+  } else {
+    smem = Layout<128>::kAlloc;
+    e = bf16 ? launch_fwd<128, true>(p, static_cast<int>(grid), s)
+             : launch_fwd<128, false>(p, static_cast<int>(grid), s);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  t_last_grid = static_cast<int>(grid);
+  t_last_smem = smem;
+  return ATTN_OK;
+}
+
+extern "C" int attn_check(void* stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  DeviceState* ds = nullptr;
+  int st = device_state(dev, &ds);
+  if (st != ATTN_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  int word = 0;
+  if (cudaMemcpy(&word, ds->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(ds->err, 0, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  if (word & kErrTimeout) return ATTN_ERR_DEVICE_TIMEOUT;
+  if (word & kErrBadSeqlens) return ATTN_ERR_BAD_SEQLENS;
+  return ATTN_OK;
+}
+
+extern "C" const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT";
+    case ATTN_ERR_BAD_SEQLENS: return "ATTN_ERR_BAD_SEQLENS";
+    default: return "ATTN_ERR_UNKNOWN";
+  }
+}
+
+extern "C" int attn_num_sms(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  DeviceState* ds = nullptr;
+  int st = device_state(dev, &ds);
+  return st == ATTN_OK ? ds->sms : st;
+}
+
+extern "C" int attn_last_launch(int* grid_ctas, int* smem_bytes) {
+  if (t_last_grid < 0) return ATTN_ERR_INVALID_ARG;
+  if (grid_ctas) *grid_ctas = t_last_grid;
+  if (smem_bytes) *smem_bytes = t_last_smem;
+  return ATTN_OK;
+}
+
+extern "C" int attn_release(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = ATTN_OK;
+  int cur = 0;
+  const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+  for (int d = 0; d < kMaxDevices; ++d) {
+    DeviceState& s = g_dev[d];
+    if (s.ready && s.err) {
+      if (cudaSetDevice(d) != cudaSuccess || cudaFree(s.err) != cudaSuccess) rc = ATTN_ERR_CUDA;
+    }
+    s = DeviceState();
+  }
+  if (have_cur) cudaSetDevice(cur);
+  cudaGetLastError();
+  return rc;
+}

@@ -1,0 +1,6 @@
+// Instantiation of the fused attention forward for head dim 64, f16 inputs.
+#include "fwd_kernel.cuh"
+
+namespace attn {
+template cudaError_t launch_fwd<64, false>(const FwdParams&, int, cudaStream_t);
+}  // namespace attn

@@ -1,0 +1,583 @@
+// Fused attention forward for sm_103a: one persistent, warp-specialised kernel.
+//
+// What it computes (per sequence b, head h, query row i):
+//   O_i   = sum_j softmax_j(scale * q_i . k_j) v_j   over the visible keys j
+//   LSE_i = ln sum_j exp(scale * q_i . k_j)
+// Definition: page "Multi-Head Attention的计算本质与性能瓶颈", §1/§2.1; causal
+// rule (key j visible iff j <= i) from §3.1 of the same page; varlen packing
+// from page "长文本处理性能断层真相", §1.  The scores are consumed tile by tile
+// with the online softmax of page "深度学习算子优化：从TFLOPS幻觉到
+// FlashAttention实战", §3 (running row max m_i, running exp-sum l_i, rescale of
+// the accumulator, one final normalisation), so S never reaches global memory.
+//
+// GB300 mapping (the pages' A100 sketches are prior art only):
+//   * work unit = (sequence, head, 256 query rows) = two 128-row query tiles
+//     that share every K/V tile; persistent grid, static stride over units,
+//     heaviest causal units first;
+//   * warp 9 (one lane) streams Q, K, V with 3-D TMA into 128-byte-swizzled
+//     shared memory, K and V each in a ring of kStages buffers;
+//   * warp 8 (one lane) issues tcgen05.mma: S_t = Q_t K^T (both operands in
+//     shared memory) and O_t += P_t V (P read from tensor memory);
+//   * warps 0-3 / 4-7 run the softmax of query tile 0 / 1, one thread per
+//     query row (= one TMEM lane), so row max and row sum need no shuffles;
+//     they write P (16-bit) over the S columns in TMEM and rescale O in TMEM
+//     only when the running max grows by more than 2^8;
+//   * TMEM: S0 | S1 | O0 | O1 columns; P_t aliases the first 64 columns of S_t.
+// Every pipeline wait is bounded: on expiry the kernel records an error in a
+// device word, tells the other roles through a shared flag and winds down.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr int kBM = 128;                 // query rows per tile (= TMEM lanes)
+constexpr int kBN = 128;                 // keys per K/V tile
+constexpr int kTiles = 2;                // query tiles per work unit
+constexpr int kUnitRows = kBM * kTiles;  // query rows per work unit
+constexpr int kThreads = 320;            // 8 softmax warps + MMA warp + load warp
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr int kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;     // rescale O only if max grows by > 2^8
+
+enum : int { kErrTimeout = 1, kErrBadSeqlens = 2 };
+
+struct FwdParams {
+  CUtensorMap tm_q;          // [rows_q, H, D] 16-bit, box 128 x 1 x 64
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  void* o;
+  float* lse;
+  const int32_t* cu_q;       // varlen only
+  const int32_t* cu_k;
+  int* err;                  // device error word (bit flags above)
+  int B, H, Sq, Sk;          // dense: per-batch lengths; varlen: total packed rows
+  int varlen, causal;
+  float scale_log2;          // scale * log2(e)
+  int scale_pos;             // scale > 0: fold the scale into the exp2 argument
+  long long timeout_ns;      // limit for any single pipeline wait
+};
+
+template <int D>
+struct Layout {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kBlk = 16384;                  // 128 rows x 128 B swizzle block
+  static constexpr int kTileBytes = (D / 64) * kBlk;  // one 128-row tile, all of D
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kTiles * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  // barrier indices
+  static constexpr int QF = 0, QE = 1, KF = 2, KE = KF + kStages, VF = KE + kStages,
+                       VE = VF + kStages, SF = VE + kStages, PF = SF + 2, OF = PF + 2,
+                       DONE = OF + 2, kNumBars = DONE + 1;
+  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;             // slack for 1024-B alignment
+  // TMEM columns
+  static constexpr uint32_t kColS = 0, kColO = 256;
+};
+
+// ------------------------------------------------------------ bounded waits
+struct Ctl {
+  volatile int* abort_flag;  // shared memory
+  int* err;
+  long long timeout_ns;
+};
+
+// Polls `bar` for the phase of the given parity.  Gives up (returning false)
+// when another role has raised the abort flag, or after c.timeout_ns, in which
+// case it raises the flag and records kErrTimeout.  With honor_abort == false
+// only the time limit applies (used to drain work already in flight).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c,
+                                         bool honor_abort = true) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((n & 15u) == 0) {
+      if (honor_abort && *c.abort_flag) return false;
+      if (static_cast<long long>(ptx::global_timer_ns() - t0) > c.timeout_ns) {
+        *c.abort_flag = 1;
+        atomicOr(c.err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// All 32 lanes wait; the warp proceeds only if every lane saw the phase.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const Ctl& c) {
+  const bool ok = wait_bar(bar, parity, c);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// ------------------------------------------------------------- work units
+struct Unit {
+  int b, h, qt;               // sequence, head, unit index within the sequence
+  int q_start, Lq, k_start, Lk;
+  int n[kTiles];              // K/V tiles visited by each query tile
+  bool valid[kTiles];         // tile holds at least one real query row
+};
+
+struct Cursor {               // forward-only walk over varlen sequences
+  int b, base, units;
+  int q_start, Lq, k_start, Lk;
+};
+
+__device__ __forceinline__ void load_seq(const FwdParams& p, Cursor& c, bool report) {
+  c.units = 0;
+  c.q_start = c.Lq = c.k_start = c.Lk = 0;
+  if (c.b >= p.B) return;
+  const int q0 = __ldg(p.cu_q + c.b), q1 = __ldg(p.cu_q + c.b + 1);
+  const int k0 = __ldg(p.cu_k + c.b), k1 = __ldg(p.cu_k + c.b + 1);
+  const bool ok = 0 <= q0 && q0 <= q1 && q1 <= p.Sq && 0 <= k0 && k0 <= k1 && k1 <= p.Sk;
+  if (!ok) {
+    if (report) atomicOr(p.err, kErrBadSeqlens);
+    return;
+  }
+  c.q_start = q0;
+  c.Lq = q1 - q0;
+  c.k_start = k0;
+  c.Lk = k1 - k0;
+  c.units = p.H * ((c.Lq + kUnitRows - 1) / kUnitRows);
+}
+
+__device__ __forceinline__ void init_cursor(const FwdParams& p, Cursor& c, bool report) {
+  c.b = 0;
+  c.base = 0;
+  if (p.varlen) load_seq(p, c, report);
+}
+
+// Decodes unit u (units are visited in increasing order by each CTA).
+// Order: dense -> (row block, batch, head), causal row blocks heaviest first;
+// varlen -> (sequence, row block, head), causal row blocks heaviest first.
+__device__ __forceinline__ bool decode_unit(const FwdParams& p, int u, Cursor& c, Unit& w,
+                                            bool report) {
+  if (!p.varlen) {
+    const int nU = (p.Sq + kUnitRows - 1) / kUnitRows;
+    const int per = p.B * p.H;
+    if (u >= per * nU) return false;
+    const int r = u / per;
+    const int rem = u - r * per;
+    w.qt = p.causal ? (nU - 1 - r) : r;
+    w.b = rem / p.H;
+    w.h = rem - w.b * p.H;
+    w.q_start = w.b * p.Sq;
+    w.Lq = p.Sq;
+    w.k_start = w.b * p.Sk;
+    w.Lk = p.Sk;
+  } else {
+    while (true) {
+      if (c.b >= p.B) return false;
+      if (u < c.base + c.units) break;
+      c.base += c.units;
+      c.b += 1;
+      load_seq(p, c, report);
+    }
+    const int rem = u - c.base;
+    const int r = rem / p.H;
+    const int nU = c.units / p.H;
+    w.h = rem - r * p.H;
+    w.qt = p.causal ? (nU - 1 - r) : r;
+    w.b = c.b;
+    w.q_start = c.q_start;
+    w.Lq = c.Lq;
+    w.k_start = c.k_start;
+    w.Lk = c.Lk;
+  }
+  const int nk = (w.Lk + kBN - 1) / kBN;
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t) {
+    const int q0 = w.qt * kUnitRows + t * kBM;
+    w.valid[t] = q0 < w.Lq;
+    // causal: rows q0..q0+127 see keys <= their index, so tiles up to the diagonal
+    w.n[t] = !w.valid[t] ? 0 : (p.causal ? min(nk, q0 / kBN + 1) : nk);
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- softmax
+// Running state of one query row.  l_p sums the 16-bit P values that enter
+// P.V (it normalises O, so rounding of P cancels between numerator and
+// denominator); l_x sums the unrounded values (it gives the logsumexp).
+struct RowState {
+  float m;    // running max, log2 units (scale * log2e * s)
+  float l_p;
+  float l_x;
+};
+
+// One K/V tile of the online softmax for the calling thread's query row.
+// S is read from TMEM (128 fp32 columns), masked (keys c > limit are invisible),
+// turned into P = 2^(scale*log2e*s - m) rounded to 16 bits and written back over
+// the first 64 columns of S.  O is rescaled in TMEM when the running max moved
+// by more than 2^kRescaleLog2; otherwise the stale max is kept for P and l,
+// which leaves the result exact.
+template <int D, bool BF16>
+__device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, int limit, float cl,
+                                             bool scale_pos, bool first, RowState& st) {
+  uint32_t r[128];
+  ptx::tmem_ld_x128(tS, r);
+  float cle = cl;
+  if (!scale_pos) {  // scale <= 0: scale first so that "max" stays a max
+    const uint64_t c2 = ptx::f2(cl, cl);
+#pragma unroll
+    for (int c = 0; c < 128; c += 2) {
+      float a, b;
+      ptx::f2_split(ptx::f2_mul(ptx::f2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), c2),
+                    a, b);
+      r[c] = __float_as_uint(a);
+      r[c + 1] = __float_as_uint(b);
+    }
+    cle = 1.0f;
+  }
+  if (limit < 127) {
+#pragma unroll
+    for (int c = 0; c < 128; ++c)
+      if (c > limit) r[c] = __float_as_uint(-INFINITY);
+  }
+  float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 128; c += 8) {
+    mx0 = ptx::max3(mx0, __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+    mx1 = ptx::max3(mx1, __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]));
+    mx2 = ptx::max3(mx2, __uint_as_float(r[c + 4]), __uint_as_float(r[c + 5]));
+    mx3 = ptx::max3(mx3, __uint_as_float(r[c + 6]), __uint_as_float(r[c + 7]));
+  }
+  const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cle;
+  const float m_new = fmaxf(st.m, m_tile);
+  const bool rescale = m_new > st.m + kRescaleLog2;  // always true on the first tile
+  const float m_use = rescale ? m_new : st.m;
+  const float m_safe = (m_use == -INFINITY) ? 0.0f : m_use;
+  const float alpha = rescale ? ptx::ex2(st.m - m_safe) : 1.0f;
+  st.m = m_use;
+
+  const uint64_t cl2 = ptx::f2(cle, cle);
+  const uint64_t nm2 = ptx::f2(-m_safe, -m_safe);
+  uint64_t lx0 = ptx::f2(0.f, 0.f), lx1 = lx0;
+  float lp0 = 0.f, lp1 = 0.f, lp2 = 0.f, lp3 = 0.f;
+  uint32_t pk[64];
+#pragma unroll
+  for (int c = 0; c < 128; c += 4) {
+    float x0, x1, x2, x3;
+    ptx::f2_split(ptx::f2_fma(ptx::f2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), cl2,
+                              nm2), x0, x1);
+    ptx::f2_split(ptx::f2_fma(ptx::f2(__uint_as_float(r[c + 2]), __uint_as_float(r[c + 3])),
+                              cl2, nm2), x2, x3);
+    const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1), p2 = ptx::ex2(x2), p3 = ptx::ex2(x3);
+    lx0 = ptx::f2_add(lx0, ptx::f2(p0, p1));
+    lx1 = ptx::f2_add(lx1, ptx::f2(p2, p3));
+    pk[c / 2] = ptx::pack2<BF16>(p0, p1);
+    pk[c / 2 + 1] = ptx::pack2<BF16>(p2, p3);
+    lp0 = ptx::add_lo16<BF16>(lp0, pk[c / 2]);
+    lp1 = ptx::add_hi16<BF16>(lp1, pk[c / 2]);
+    lp2 = ptx::add_lo16<BF16>(lp2, pk[c / 2 + 1]);
+    lp3 = ptx::add_hi16<BF16>(lp3, pk[c / 2 + 1]);
+  }
+  ptx::tmem_st_x64(tS, pk);
+  float a0, a1, b0, b1;
+  ptx::f2_split(lx0, a0, a1);
+  ptx::f2_split(lx1, b0, b1);
+  st.l_x = st.l_x * alpha + ((a0 + a1) + (b0 + b1));
+  st.l_p = st.l_p * alpha + ((lp0 + lp1) + (lp2 + lp3));
+
+  if (!first && __any_sync(0xffffffffu, rescale)) {
+    const uint64_t al2 = ptx::f2(alpha, alpha);
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      uint32_t o[32];
+      ptx::tmem_ld_x32(tO + c0, o);
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        float a, b;
+        ptx::f2_split(
+            ptx::f2_mul(ptx::f2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), al2), a, b);
+        o[i] = __float_as_uint(a);
+        o[i + 1] = __float_as_uint(b);
+      }
+      ptx::tmem_st_x32(tO + c0, o);
+    }
+  }
+  ptx::tmem_wait_st();
+}
+
+template <int D, bool BF16>
+__device__ void softmax_role(const FwdParams& p, int t, uint32_t tmem, uint32_t bars,
+                             const Ctl& ctl) {
+  using L = Layout<D>;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+  const int row = quarter * 32 + lane;
+  const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
+  const uint32_t tS = tmem + lane_bits + L::kColS + t * 128;
+  const uint32_t tO = tmem + lane_bits + L::kColO + t * D;
+  const uint32_t bar_s = bars + 8 * (L::SF + t);
+  const uint32_t bar_p = bars + 8 * (L::PF + t);
+  const uint32_t bar_o = bars + 8 * (L::OF + t);
+  uint32_t s_cnt = 0, o_cnt = 0;
+  using out_t = uint16_t;
+  out_t* const O = static_cast<out_t*>(p.o);
+
+  Cursor cur;
+  init_cursor(p, cur, false);
+  Unit w;
+  for (int u = blockIdx.x; decode_unit(p, u, cur, w, false); u += gridDim.x) {
+    if (!(t == 0 ? w.valid[0] : w.valid[1])) continue;
+    const int q0 = w.qt * kUnitRows + t * kBM;
+    const int qrow = q0 + row;
+    const bool row_ok = qrow < w.Lq;
+    const int n = t == 0 ? w.n[0] : w.n[1];
+    const long long orow = (static_cast<long long>(w.q_start) + qrow) * p.H + w.h;
+    const long long lidx = p.varlen
+                               ? static_cast<long long>(w.h) * p.Sq + w.q_start + qrow
+                               : (static_cast<long long>(w.b) * p.H + w.h) * p.Sq + qrow;
+    RowState rs{-INFINITY, 0.0f, 0.0f};
+    if (n > 0) {
+      const int diag = q0 / kBN;
+      for (int j = 0; j < n; ++j) {
+        if (!wait_bar_warp(bar_s, s_cnt & 1u, ctl)) return;
+        ++s_cnt;
+        ptx::tc_fence_after();
+        int limit = (p.causal && j == diag) ? row : 127;
+        limit = min(limit, w.Lk - j * kBN - 1);
+        softmax_step<D, BF16>(tS, tO, limit, p.scale_log2, p.scale_pos != 0, j == 0, rs);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_p);
+      }
+      if (!wait_bar_warp(bar_o, o_cnt & 1u, ctl)) return;
+      ++o_cnt;
+      ptx::tc_fence_after();
+      const float inv_l = rs.l_p > 0.0f ? 1.0f / rs.l_p : 0.0f;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        ptx::tmem_ld_x32(tO + c0, o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = ptx::pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
+                                   __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(O + orow * D + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+    } else if (row_ok) {  // no visible key at all: O = 0, LSE = -inf
+      uint4* dst = reinterpret_cast<uint4*>(O + orow * D);
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (row_ok) {
+      p.lse[lidx] = rs.l_x > 0.0f ? (rs.m + ptx::lg2(rs.l_x)) * 0.69314718055994531f : -INFINITY;
+    }
+  }
+}
+
+// -------------------------------------------------------------------- MMA
+template <int D, bool BF16>
+__device__ void mma_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint32_t bars,
+                         const Ctl& ctl) {
+  using L = Layout<D>;
+  constexpr int NS = L::kStages;
+  constexpr uint32_t kIdS = ptx::idesc_f16_f32acc(BF16, kBM, kBN, false);
+  constexpr uint32_t kIdPV = ptx::idesc_f16_f32acc(BF16, kBM, D, true);
+  auto bar = [&](int i) { return bars + 8u * i; };
+  uint32_t kv_it = 0, q_it = 0, p_cnt[kTiles] = {0, 0};
+
+  Cursor cur;
+  init_cursor(p, cur, false);
+  Unit w;
+  for (int u = blockIdx.x; decode_unit(p, u, cur, w, false); u += gridDim.x) {
+    const int nmax = max(w.n[0], w.n[1]);
+    if (nmax == 0) continue;
+    if (!wait_bar(bar(L::QF), q_it & 1u, ctl)) return;
+    ptx::tc_fence_after();
+    for (int j = 0; j <= nmax; ++j) {
+#pragma unroll
+      for (int t = 0; t < kTiles; ++t) {
+        const uint32_t tS = tmem + L::kColS + t * 128;
+        const uint32_t tO = tmem + L::kColO + t * D;
+        if (j >= 1 && j - 1 < w.n[t]) {  // O_t += P_t(j-1) V(j-1)
+          if (!wait_bar(bar(L::PF + t), p_cnt[t] & 1u, ctl)) return;
+          ++p_cnt[t];
+          const uint32_t it = kv_it + j - 1;
+          const uint32_t st = it % NS;
+          if (!wait_bar(bar(L::VF + st), (it / NS) & 1u, ctl)) return;
+          ptx::tc_fence_after();
+          const uint32_t vbase = smem + L::kVOff + st * L::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks) {
+            // V is MN-major: 16 keys = 2 swizzle atoms of 8 keys x 128 B;
+            // LBO = next 64-column block of D, SBO = next 8 keys.
+            const uint64_t bdesc = ptx::desc_sw128(vbase + ks * 2048, L::kBlk, 1024);
+            ptx::mma_ts(tO, tS + ks * 8, bdesc, kIdPV, (j - 1 > 0 || ks > 0) ? 1u : 0u);
+          }
+          if (t == 1 || j - 1 >= w.n[1]) ptx::mma_commit(bar(L::VE + st));
+          if (j - 1 == w.n[t] - 1) ptx::mma_commit(bar(L::OF + t));
+        }
+        if (j < w.n[t]) {  // S_t(j) = Q_t K(j)^T
+          const uint32_t it = kv_it + j;
+          const uint32_t st = it % NS;
+          if (!wait_bar(bar(L::KF + st), (it / NS) & 1u, ctl)) return;
+          ptx::tc_fence_after();
+          const uint32_t qbase = smem + L::kQOff + t * L::kTileBytes;
+          const uint32_t kbase = smem + L::kKOff + st * L::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            // K-major, 16 elements = 32 B step inside the 128-B swizzle row.
+            const uint32_t off = (ks >> 2) * L::kBlk + (ks & 3) * 32;
+            const uint64_t adesc = ptx::desc_sw128(qbase + off, 16, 1024);
+            const uint64_t bdesc = ptx::desc_sw128(kbase + off, 16, 1024);
+            ptx::mma_ss(tS, adesc, bdesc, kIdS, ks > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(bar(L::SF + t));
+          if (t == 1 || j >= w.n[1]) ptx::mma_commit(bar(L::KE + st));
+        }
+      }
+      if (j == nmax - 1) ptx::mma_commit(bar(L::QE));
+    }
+    kv_it += nmax;
+    ++q_it;
+  }
+  // make sure every issued tcgen05 operation retired before TMEM is freed
+}
+
+template <int D, bool BF16>
+__device__ void mma_role(const FwdParams& p, uint32_t smem, uint32_t tmem, uint32_t bars,
+                         const Ctl& ctl) {
+  mma_loop<D, BF16>(p, smem, tmem, bars, ctl);
+  // Every tcgen05 operation issued so far must retire before TMEM is freed,
+  // also when the loop was abandoned.
+  const uint32_t done = bars + 8u * Layout<D>::DONE;
+  ptx::mma_commit(done);
+  wait_bar(done, 0, ctl, false);
+}
+
+// ------------------------------------------------------------------- load
+template <int D>
+__device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bars, const Ctl& ctl,
+                          uint32_t& kv_it, uint32_t& q_it) {
+  using L = Layout<D>;
+  constexpr int NS = L::kStages;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  Cursor cur;
+  init_cursor(p, cur, true);
+  Unit w;
+  for (int u = blockIdx.x; decode_unit(p, u, cur, w, true); u += gridDim.x) {
+    const int nmax = max(w.n[0], w.n[1]);
+    if (nmax == 0) continue;
+    if (q_it > 0 && !wait_bar(bar(L::QE), (q_it - 1) & 1u, ctl)) return;
+    ptx::mbar_arrive_expect_tx(bar(L::QF), kTiles * L::kTileBytes);
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t)
+#pragma unroll
+      for (int blk = 0; blk < D / 64; ++blk)
+        ptx::tma_load_3d(smem + L::kQOff + t * L::kTileBytes + blk * L::kBlk, &p.tm_q,
+                         bar(L::QF), blk * 64, w.h, w.q_start + w.qt * kUnitRows + t * kBM);
+    ++q_it;
+    for (int j = 0; j < nmax; ++j) {
+      const uint32_t it = kv_it + j;
+      const uint32_t st = it % NS;
+      const int krow = w.k_start + j * kBN;
+      if (it >= NS && !wait_bar(bar(L::KE + st), (it / NS - 1) & 1u, ctl)) return;
+      ptx::mbar_arrive_expect_tx(bar(L::KF + st), L::kTileBytes);
+#pragma unroll
+      for (int blk = 0; blk < D / 64; ++blk)
+        ptx::tma_load_3d(smem + L::kKOff + st * L::kTileBytes + blk * L::kBlk, &p.tm_k,
+                         bar(L::KF + st), blk * 64, w.h, krow);
+      if (it >= NS && !wait_bar(bar(L::VE + st), (it / NS - 1) & 1u, ctl)) return;
+      ptx::mbar_arrive_expect_tx(bar(L::VF + st), L::kTileBytes);
+#pragma unroll
+      for (int blk = 0; blk < D / 64; ++blk)
+        ptx::tma_load_3d(smem + L::kVOff + st * L::kTileBytes + blk * L::kBlk, &p.tm_v,
+                         bar(L::VF + st), blk * 64, w.h, krow);
+    }
+    kv_it += nmax;
+  }
+}
+
+template <int D>
+__device__ void load_role(const FwdParams& p, uint32_t smem, uint32_t bars, const Ctl& ctl) {
+  using L = Layout<D>;
+  constexpr uint32_t NS = L::kStages;
+  uint32_t kv_it = 0, q_it = 0;
+  load_loop<D>(p, smem, bars, ctl, kv_it, q_it);
+  // Wait for the last copy issued into each buffer so no TMA write can land
+  // after the CTA exits (normally these phases completed long ago).
+  if (q_it > 0) wait_bar(bars + 8u * L::QF, (q_it - 1) & 1u, ctl, false);
+  for (uint32_t st = 0; st < NS && st < kv_it; ++st) {
+    const uint32_t last = st + ((kv_it - 1 - st) / NS) * NS;
+    wait_bar(bars + 8u * (L::KF + st), (last / NS) & 1u, ctl, false);
+    wait_bar(bars + 8u * (L::VF + st), (last / NS) & 1u, ctl, false);
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t smem = (raw + 1023u) & ~1023u;
+  uint8_t* const base = smem_raw + (smem - raw);
+  const uint32_t bars = smem + L::kBarOff;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base + L::kMiscOff);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(base + L::kMiscOff + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::kNumBars; ++i)
+      ptx::mbar_init(bars + 8u * i, (i == L::PF || i == L::PF + 1) ? kBM : 1u);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    ptx::tma_prefetch_desc(&p.tm_q);
+    ptx::tma_prefetch_desc(&p.tm_k);
+    ptx::tma_prefetch_desc(&p.tm_v);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Ctl ctl{abort_flag, p.err, p.timeout_ns};
+
+  if (warp < kMmaWarp) {
+    softmax_role<D, BF16>(p, warp >> 2, tmem, bars, ctl);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) mma_role<D, BF16>(p, smem, tmem, bars, ctl);
+  } else if (lane == 0) {
+    load_role<D>(p, smem, bars, ctl);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int D, bool BF16>
+cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream) {
+  const void* fn = reinterpret_cast<const void*>(&attn_fwd_kernel<D, BF16>);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Layout<D>::kAlloc);
+  if (e != cudaSuccess) return e;
+  void* args[] = {const_cast<FwdParams*>(&p)};
+  return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, Layout<D>::kAlloc, stream);
+}
+
+}  // namespace attn

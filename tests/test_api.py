@@ -1,0 +1,123 @@
+"""Host-side checks of the C ABI and the Python binding (no GPU needed).
+
+Argument validation in attn_fwd runs before any CUDA call, so invalid calls can
+be exercised on a machine without a GPU: the fake pointer values below are
+never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import scaled_dot_product_tcgen05_gb300 as pkg
+from scaled_dot_product_tcgen05_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return pkg.load_library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    fns = header_functions()
+    assert "attn_fwd" in fns and "attn_check" in fns and "attn_status_string" in fns
+    assert set(fns) == set(pkg.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    # also check the dynamic symbol table directly
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", build_lib.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    for name in header_functions():
+        assert re.search(rf"\bT {name}$", out, flags=re.M), name
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "ATTN_OK"), (-1, "ATTN_ERR_INVALID_ARG"), (-2, "ATTN_ERR_UNSUPPORTED"),
+                       (-3, "ATTN_ERR_MISALIGNED"), (-4, "ATTN_ERR_CUDA"),
+                       (-5, "ATTN_ERR_DEVICE_TIMEOUT"), (-6, "ATTN_ERR_BAD_SEQLENS")]:
+        assert lib.attn_status_string(code).decode() == name
+    assert lib.attn_status_string(123).decode() == "ATTN_ERR_UNKNOWN"
+
+
+A = 0x10000  # fake, 16-byte aligned addresses: validation fails before any use
+
+
+def call(lib, **kw):
+    args = dict(q=A, k=A + 0x100, v=A + 0x200, o=A + 0x300, lse=A + 0x400, B=1, H=2, Sq=128,
+                Sk=128, D=64, scale=0.125, causal=0, cq=0, ck=0, dtype=0)
+    args.update(kw)
+    return pkg.attn_fwd_raw(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"],
+                            args["H"], args["Sq"], args["Sk"], args["D"], args["scale"],
+                            args["causal"], args["cq"], args["ck"], args["dtype"], 0)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=96), pkg.ATTN_ERR_UNSUPPORTED),
+    (dict(D=256), pkg.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=2), pkg.ATTN_ERR_UNSUPPORTED),
+    (dict(B=-1), pkg.ATTN_ERR_INVALID_ARG),
+    (dict(H=0), pkg.ATTN_ERR_INVALID_ARG),
+    (dict(Sq=-5), pkg.ATTN_ERR_INVALID_ARG),
+    (dict(Sk=0), pkg.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), pkg.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), pkg.ATTN_ERR_INVALID_ARG),
+    (dict(cq=A + 0x500), pkg.ATTN_ERR_INVALID_ARG),
+    (dict(ck=A + 0x500), pkg.ATTN_ERR_INVALID_ARG),
+    (dict(q=0), pkg.ATTN_ERR_INVALID_ARG),
+    (dict(lse=0), pkg.ATTN_ERR_INVALID_ARG),
+    (dict(q=A + 8), pkg.ATTN_ERR_MISALIGNED),
+    (dict(o=A + 2), pkg.ATTN_ERR_MISALIGNED),
+    (dict(lse=A + 2), pkg.ATTN_ERR_MISALIGNED),
+    (dict(cq=A + 0x502, ck=A + 0x600), pkg.ATTN_ERR_MISALIGNED),
+    (dict(B=1 << 16, Sq=1 << 16), pkg.ATTN_ERR_INVALID_ARG),
+])
+def test_invalid_arguments_rejected_before_launch(lib, kw, code):
+    assert call(lib, **kw) == code
+
+
+def test_empty_problem_is_a_noop(lib):
+    assert call(lib, B=0) == pkg.ATTN_OK
+    assert call(lib, Sq=0) == pkg.ATTN_OK
+    assert call(lib, B=0, q=0, k=0, v=0, o=0, lse=0) == pkg.ATTN_OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
+def test_no_device_fails_loudly(lib):
+    st = call(lib)
+    assert st in (pkg.ATTN_ERR_CUDA, pkg.ATTN_ERR_UNSUPPORTED)
+    assert lib.attn_num_sms() < 0
+    with pytest.raises(ValueError):
+        pkg.attn_fwd(torch.zeros(1, 128, 2, 64, dtype=torch.float16),
+                     torch.zeros(1, 128, 2, 64, dtype=torch.float16),
+                     torch.zeros(1, 128, 2, 64, dtype=torch.float16))
+
+
+def test_missing_library_raises(tmp_path):
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        pkg.load_library(str(tmp_path / "missing.so"))
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg_dir = os.path.join(ROOT, "scaled_dot_product_tcgen05_gb300")
+    pat = re.compile(r"^\s*(import\s+oracle|from\s+oracle)|sdpa_oracle|#include.*oracle", re.M)
+    for dirpath, _, files in os.walk(pkg_dir):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp", ".c")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert not pat.search(text), f

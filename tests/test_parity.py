@@ -1,0 +1,192 @@
+"""GPU parity: the CUDA path against the fp64 CPU oracle on the same seeded inputs.
+
+All calls go through the C ABI (ctypes binding).  Workloads follow the five
+families of the attention-forward study (tiny, 512, 2K with a peaked draw,
+packed varlen, long context) plus edge cases: ragged tails, Sq != Sk, empty
+and single-token sequences, zero and negative scale, poisoned output buffers.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import scaled_dot_product_tcgen05_gb300 as pkg
+from scaled_dot_product_tcgen05_gb300 import workloads as W
+from oracle.sdpa_oracle import attention_dense, attention_varlen
+from parity_helpers import compare, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+WL = W.standard_workloads()
+SMALL = [n for n in WL if not n.startswith("long")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkg.load_library()
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_workload_parity(name):
+    wl = WL[name]
+    inp = W.make_inputs(wl)
+    o, lse = run_gpu(inp["q"], inp["k"], inp["v"], wl.causal, wl.scale, inp["cu_seqlens_q"],
+                     inp["cu_seqlens_k"])
+    if wl.varlen:
+        o_ref, l_ref = attention_varlen(inp["q"], inp["k"], inp["v"], inp["cu_seqlens_q"],
+                                        inp["cu_seqlens_k"], wl.scale, wl.causal)
+    else:
+        o_ref, l_ref = attention_dense(inp["q"], inp["k"], inp["v"], wl.scale, wl.causal)
+    compare(o, lse, o_ref, l_ref, what=name)
+
+
+@pytest.mark.parametrize("name", ["long64k_causal", "long128k_causal"])
+def test_long_context_sampled_rows(name):
+    """Full GPU run; the oracle checks 256 seeded rows on 4 seeded heads."""
+    wl = WL[name]
+    heads, rows = W.sampled_heads_rows(wl)
+    inp = W.make_inputs(wl)
+    o, lse = run_gpu(inp["q"], inp["k"], inp["v"], True, wl.scale)
+    o_ref, l_ref = attention_dense(inp["q"], inp["k"], inp["v"], wl.scale, True, heads=heads,
+                                   rows=rows)
+    o_s = o[:, rows][:, :, heads].float().cpu().numpy()
+    l_s = lse[:, heads][:, :, rows].cpu().numpy()
+    compare(o_s, l_s, o_ref[:, rows][:, :, heads], l_ref[:, heads][:, :, rows], what=name)
+    # every output is finite, and rows of the unsampled heads are plausible
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+def _dense_case(seed, B, H, Sq, Sk, D, dtype, std=1.0):
+    g = torch.Generator().manual_seed(seed)
+    mk = lambda S: (torch.randn(B, S, H, D, generator=g) * std).to(dtype)  # noqa: E731
+    return mk(Sq), mk(Sk), mk(Sk)
+
+
+EDGE = [
+    # (B, H, Sq, Sk, D, dtype, causal)
+    (1, 1, 1, 1, 64, torch.float16, False),
+    (1, 1, 1, 1, 128, torch.bfloat16, True),
+    (2, 3, 127, 127, 64, torch.bfloat16, True),
+    (2, 3, 129, 129, 128, torch.float16, True),
+    (1, 2, 2050, 2050, 64, torch.float16, True),
+    (1, 2, 2050, 2050, 128, torch.bfloat16, False),
+    (2, 2, 300, 77, 128, torch.bfloat16, False),
+    (2, 2, 77, 300, 64, torch.float16, False),
+    (2, 2, 300, 77, 64, torch.bfloat16, True),
+    (2, 2, 77, 300, 128, torch.float16, True),
+    (3, 5, 256, 256, 128, torch.float16, False),
+    (1, 4, 385, 1000, 128, torch.bfloat16, False),
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=lambda c: "B{}H{}q{}k{}D{}{}{}".format(
+    c[0], c[1], c[2], c[3], c[4], "bf" if c[5] == torch.bfloat16 else "fp", "c" if c[6] else ""))
+def test_edge_shapes(case):
+    B, H, Sq, Sk, D, dt, causal = case
+    q, k, v = _dense_case(Sq * 7 + Sk, B, H, Sq, Sk, D, dt)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_gpu(q, k, v, causal, scale)
+    o_ref, l_ref = attention_dense(q, k, v, scale, causal)
+    compare(o, lse, o_ref, l_ref, what=str(case))
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.2, 0.9])
+def test_scale_values(scale):
+    q, k, v = _dense_case(3, 1, 2, 200, 200, 64, torch.float16)
+    for causal in (False, True):
+        o, lse = run_gpu(q, k, v, causal, scale)
+        o_ref, l_ref = attention_dense(q, k, v, scale, causal)
+        compare(o, lse, o_ref, l_ref, what=f"scale={scale} causal={causal}")
+
+
+def _varlen(seed, lens_q, lens_k, H, D, dtype):
+    g = torch.Generator().manual_seed(seed)
+    cq = W.cu_seqlens_from_lengths(lens_q)
+    ck = W.cu_seqlens_from_lengths(lens_k)
+    q = torch.randn(int(cq[-1]), H, D, generator=g).to(dtype)
+    k = torch.randn(max(int(ck[-1]), 1), H, D, generator=g).to(dtype)
+    v = torch.randn(max(int(ck[-1]), 1), H, D, generator=g).to(dtype)
+    return q, k, v, cq, ck
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D,dt", [(64, torch.float16), (128, torch.bfloat16)])
+def test_varlen_edges(causal, D, dt):
+    lens_q = [1, 0, 300, 129, 5, 256, 1000]
+    lens_k = [1, 7, 300, 129, 0, 100, 1000]
+    q, k, v, cq, ck = _varlen(11, lens_q, lens_k, 3, D, dt)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_gpu(q, k, v, causal, scale, cq, ck)
+    o_ref, l_ref = attention_varlen(q, k, v, cq, ck, scale, causal)
+    compare(o, lse, o_ref, l_ref, what=f"varlen causal={causal} D={D}")
+    # the sequence with no keys: O = 0 exactly, LSE = -inf
+    a, b = int(cq[4]), int(cq[5])
+    assert torch.all(o[a:b] == 0) and torch.all(torch.isneginf(lse[:, a:b]))
+
+
+def test_poisoned_outputs_and_guard_bands():
+    """Writes land only on valid rows: guards and rows outside every sequence keep NaN."""
+    H, D, dt = 2, 128, torch.bfloat16
+    lens = [130, 3, 250]
+    q, k, v, cq, ck = _varlen(12, lens, lens, H, D, dt)
+    Tq = int(cq[-1])
+    pad_rows = 40                      # rows after the last sequence: not owned by anyone
+    dev = torch.device("cuda:0")
+    qd = torch.cat([q, torch.randn(pad_rows, H, D).to(dt)]).to(dev)
+    kd, vd = k.to(dev), v.to(dev)
+    guard = 4096
+    o_buf = torch.full(((Tq + pad_rows) * H * D + 2 * guard,), float("nan"), dtype=dt, device=dev)
+    l_buf = torch.full((H * (Tq + pad_rows) + 2 * guard,), float("nan"), device=dev)
+    o = o_buf[guard:guard + (Tq + pad_rows) * H * D].view(Tq + pad_rows, H, D)
+    lse = l_buf[guard:guard + H * (Tq + pad_rows)].view(H, Tq + pad_rows)
+    pkg.attn_fwd(qd, kd, vd, causal=True, cu_seqlens_q=cq.to(dev), cu_seqlens_k=ck.to(dev),
+                 out=o, lse=lse)
+    assert pkg.attn_check() == pkg.ATTN_OK
+    assert torch.isnan(o_buf[:guard]).all() and torch.isnan(o_buf[-guard:]).all()
+    assert torch.isnan(l_buf[:guard]).all() and torch.isnan(l_buf[-guard:]).all()
+    assert torch.isnan(o[Tq:]).all() and torch.isnan(lse[:, Tq:]).all()
+    o_ref, l_ref = attention_varlen(q, k, v, cq, ck, 1 / math.sqrt(D), True)
+    compare(o[:Tq], lse[:, :Tq], o_ref, l_ref, what="poisoned")
+
+
+def test_bad_cu_seqlens_reported():
+    H, D, dt = 2, 64, torch.float16
+    dev = torch.device("cuda:0")
+    q = torch.randn(300, H, D).to(dt).to(dev)
+    cu = torch.tensor([0, 200, 100, 300], dtype=torch.int32, device=dev)  # decreasing
+    o, lse = pkg.attn_fwd(q, q, q, cu_seqlens_q=cu, cu_seqlens_k=cu)
+    assert pkg.attn_check() == pkg.ATTN_ERR_BAD_SEQLENS
+    cu2 = torch.tensor([0, 100, 400], dtype=torch.int32, device=dev)  # past the end
+    pkg.attn_fwd(q, q, q, cu_seqlens_q=cu2, cu_seqlens_k=cu2)
+    assert pkg.attn_check() == pkg.ATTN_ERR_BAD_SEQLENS
+    # the context stays usable and the next call is clean
+    qc, kc, vc = _dense_case(1, 1, 2, 128, 128, 64, torch.float16)
+    o, lse = run_gpu(qc, kc, vc, False, 0.125)
+    o_ref, l_ref = attention_dense(qc, kc, vc, 0.125, False)
+    compare(o, lse, o_ref, l_ref)
+
+
+def test_deterministic_and_stream_ordered():
+    q, k, v = _dense_case(5, 2, 4, 1024, 1024, 128, torch.bfloat16)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o1, l1 = run_gpu(q, k, v, True, 0.088, stream=s)
+        o2, l2 = run_gpu(q, k, v, True, 0.088, stream=s)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_host_and_misplaced_pointers_rejected():
+    q = torch.randn(1, 128, 2, 64).half()  # host memory
+    st = pkg.attn_fwd_raw(q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(),
+                          1, 2, 128, 128, 64, 0.125, False, 0, 0, 0, 0)
+    assert st == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_grid_is_persistent():
+    q, k, v = _dense_case(6, 1, 32, 4096, 4096, 128, torch.bfloat16)
+    run_gpu(q, k, v, True, 0.088)
+    grid, smem = pkg.last_launch()
+    assert grid == pkg.num_sms() and smem <= 232448
