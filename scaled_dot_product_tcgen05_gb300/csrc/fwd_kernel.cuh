@@ -12,8 +12,8 @@
 //
 // GB300 mapping (the pages' A100 sketches are prior art only):
 //   * work unit = (sequence, head, 256 query rows) = two 128-row query tiles
-//     that share every K/V tile; persistent grid, static stride over units,
-//     heaviest causal units first;
+//     that share every K/V tile; persistent grid, units dealt in snake order,
+//     head-major with the heaviest causal units of each head first;
 //   * warp 9 (one lane) streams Q, K, V with 3-D TMA into 128-byte-swizzled
 //     shared memory, K and V each in a ring of kStages buffers;
 //   * warp 8 (one lane) issues tcgen05.mma: S_t = Q_t K^T (both operands in
@@ -156,19 +156,21 @@ __device__ __forceinline__ void init_cursor(const FwdParams& p, Cursor& c, bool 
 }
 
 // Decodes unit u (units are visited in increasing order by each CTA).
-// Order: dense -> (row block, batch, head), causal row blocks heaviest first;
-// varlen -> (sequence, row block, head), causal row blocks heaviest first.
+// Order: (sequence, head) outer, 256-row block inner, heaviest causal blocks
+// first.  Keeping one head's blocks together keeps the K/V tiles that the
+// concurrently running CTAs stream within L2 (one head of a 64K-token
+// sequence is 32 MB); dealing the units to CTAs in a snake order (next
+// function) keeps the per-CTA work balanced.
 __device__ __forceinline__ bool decode_unit(const FwdParams& p, int u, Cursor& c, Unit& w,
                                             bool report) {
   if (!p.varlen) {
     const int nU = (p.Sq + kUnitRows - 1) / kUnitRows;
-    const int per = p.B * p.H;
-    if (u >= per * nU) return false;
-    const int r = u / per;
-    const int rem = u - r * per;
-    w.qt = p.causal ? (nU - 1 - r) : r;
-    w.b = rem / p.H;
-    w.h = rem - w.b * p.H;
+    if (u >= p.B * p.H * nU) return false;
+    const int bh = u / nU;
+    const int i = u - bh * nU;
+    w.qt = p.causal ? (nU - 1 - i) : i;
+    w.b = bh / p.H;
+    w.h = bh - w.b * p.H;
     w.q_start = w.b * p.Sq;
     w.Lq = p.Sq;
     w.k_start = w.b * p.Sk;
@@ -182,10 +184,10 @@ __device__ __forceinline__ bool decode_unit(const FwdParams& p, int u, Cursor& c
       load_seq(p, c, report);
     }
     const int rem = u - c.base;
-    const int r = rem / p.H;
     const int nU = c.units / p.H;
-    w.h = rem - r * p.H;
-    w.qt = p.causal ? (nU - 1 - r) : r;
+    w.h = rem / nU;
+    const int i = rem - w.h * nU;
+    w.qt = p.causal ? (nU - 1 - i) : i;
     w.b = c.b;
     w.q_start = c.q_start;
     w.Lq = c.Lq;
@@ -201,6 +203,15 @@ __device__ __forceinline__ bool decode_unit(const FwdParams& p, int u, Cursor& c
     w.n[t] = !w.valid[t] ? 0 : (p.causal ? min(nk, q0 / kBN + 1) : nk);
   }
   return true;
+}
+
+// The k-th unit of this CTA: units are dealt in rounds of gridDim.x, left to
+// right in even rounds and right to left in odd rounds, so that the CTA that
+// got the heaviest unit of one round gets the lightest of the next.
+__device__ __forceinline__ int unit_of(int k) {
+  const int g = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  return k * g + ((k & 1) ? (g - 1 - c) : c);
 }
 
 // ---------------------------------------------------------------- softmax
@@ -328,7 +339,7 @@ __device__ void softmax_role(const FwdParams& p, int t, uint32_t tmem, uint32_t 
   Cursor cur;
   init_cursor(p, cur, false);
   Unit w;
-  for (int u = blockIdx.x; decode_unit(p, u, cur, w, false); u += gridDim.x) {
+  for (int k = 0; decode_unit(p, unit_of(k), cur, w, false); ++k) {
     if (!(t == 0 ? w.valid[0] : w.valid[1])) continue;
     const int q0 = w.qt * kUnitRows + t * kBM;
     const int qrow = q0 + row;
@@ -396,7 +407,7 @@ __device__ void mma_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint3
   Cursor cur;
   init_cursor(p, cur, false);
   Unit w;
-  for (int u = blockIdx.x; decode_unit(p, u, cur, w, false); u += gridDim.x) {
+  for (int k = 0; decode_unit(p, unit_of(k), cur, w, false); ++k) {
     const int nmax = max(w.n[0], w.n[1]);
     if (nmax == 0) continue;
     if (!wait_bar(bar(L::QF), q_it & 1u, ctl)) return;
@@ -472,7 +483,7 @@ __device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bars, cons
   Cursor cur;
   init_cursor(p, cur, true);
   Unit w;
-  for (int u = blockIdx.x; decode_unit(p, u, cur, w, true); u += gridDim.x) {
+  for (int k = 0; decode_unit(p, unit_of(k), cur, w, true); ++k) {
     const int nmax = max(w.n[0], w.n[1]);
     if (nmax == 0) continue;
     if (q_it > 0 && !wait_bar(bar(L::QE), (q_it - 1) & 1u, ctl)) return;
