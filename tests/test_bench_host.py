@@ -1,0 +1,81 @@
+"""Host-side logic of bench.py on the CPU: replica timing over ranks (gloo, 2 ranks),
+FLOP accounting and the reference-arm JSON contract."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    ws, r = bench.init_dist("gloo")
+    t = bench.max_over_ranks(10.0 + 5.0 * rank)
+    bench.barrier()
+    q.put((r, ws, t))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_two_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == [(0, 2, 15.0), (1, 2, 15.0)]
+
+
+def test_max_over_ranks_single_process_is_identity():
+    assert bench.max_over_ranks(3.5) == 3.5
+
+
+def test_workload_info_flops_and_bytes():
+    from scaled_dot_product_tcgen05_gb300 import workloads as W
+    wl = W.standard_workloads()["long64k_causal"]
+    flops, nbytes, cfg = bench.workload_info(wl)
+    assert flops == 4 * 32 * 65536 ** 2 * 128 / 2
+    assert nbytes == 65536 * 32 * 128 * 2 * 4 + 65536 * 32 * 4
+    assert cfg["workload"] == "long64k_causal"
+
+
+def test_reference_arm_json_contract():
+    env = dict(os.environ, PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_causal", "--steps", "1", "--warmup", "3",
+                        "--ref-rows", "16"], capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    env = dict(os.environ, PYTHONPATH=ROOT, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_causal"], capture_output=True, text=True, env=env,
+                       timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == ""
