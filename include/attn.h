@@ -101,6 +101,34 @@ int attn_num_sms(void);
 int attn_last_launch(int* grid_ctas, int* smem_bytes);
 
 /*
+ * attn_fwd_noalloc -- attn_fwd for callers that must not allocate device memory.
+ * (The pages have no counterpart; this is an integration entry point.)
+ *
+ * Same arguments, layouts and argument errors as attn_fwd, plus device_status.
+ * attn_fwd cudaMalloc's a 4-byte device error word on its first call on a
+ * device; a caller whose framework owns all device memory through its own
+ * allocator, or that cannot accept cudaMalloc's implicit synchronisation,
+ * cannot allow that.  This call runs the same kernel with its scratch in a
+ * fixed 256-byte static device array (held by every GPU that loads the library
+ * until exit) and calls no cudaMalloc, cudaFree or other allocating routine.
+ *   device_status  optional host pointer.  NULL: the call stays asynchronous
+ *                  and device-side errors are not reported.  Non-NULL: the call
+ *                  waits for `stream` and stores ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT
+ *                  or ATTN_ERR_BAD_SEQLENS there.
+ * The scratch needed by a call (one error word, any problem size) is checked
+ * against the array's 256 bytes; a call needing more returns
+ * ATTN_ERR_INVALID_ARG.  All calls on a device share the array and it keeps the
+ * last call's contents: each call clears its error word on `stream` first, and
+ * calls whose kernels overlap on the GPU race on it.  The first call on a
+ * device looks up the array's address with that device current; make it before
+ * any stream capture on that device.
+ */
+int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int Sq, int Sk, int D, float scale, int causal,
+                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                     int dtype, void* stream, int* device_status);
+
+/*
  * attn_release -- free the library-owned per-device state (the error word) of
  * every device it was created on.  Call only when no attn_fwd launch is in
  * flight.  Later calls recreate the state.

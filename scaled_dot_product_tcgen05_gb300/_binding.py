@@ -28,7 +28,7 @@ ATTN_ERR_BAD_SEQLENS = -6
 DTYPE_CODES = {torch.float16: 0, torch.bfloat16: 1}
 
 EXPORTED = ("attn_fwd", "attn_check", "attn_status_string", "attn_num_sms",
-            "attn_last_launch", "attn_release")
+            "attn_last_launch", "attn_release", "attn_fwd_noalloc")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None

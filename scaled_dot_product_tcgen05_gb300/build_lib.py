@@ -21,7 +21,8 @@ LIB_NAME = "libattn_tcgen05.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "fwd_d64_f16.cu", "fwd_d64_bf16.cu", "fwd_d128_f16.cu", "fwd_d128_bf16.cu"]
+SOURCES = ["api.cu", "noalloc.cu", "fwd_d64_f16.cu", "fwd_d64_bf16.cu", "fwd_d128_f16.cu",
+           "fwd_d128_bf16.cu"]
 
 
 def _nvcc() -> str:
