@@ -404,6 +404,14 @@ __device__ void mma_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint3
   auto bar = [&](int i) { return bars + 8u * i; };
   uint32_t kv_it = 0, q_it = 0, p_cnt[kTiles] = {0, 0};
 
+  // Descriptor templates: only the 14-bit start-address field (bits 0-13,
+  // address >> 4) changes between operands, so per-MMA descriptors are formed
+  // by adding (offset >> 4) to a template built from the buffer's base.
+  const uint64_t dq[kTiles] = {ptx::desc_sw128(smem + L::kQOff, 16, 1024),
+                               ptx::desc_sw128(smem + L::kQOff + L::kTileBytes, 16, 1024)};
+  const uint64_t dk0 = ptx::desc_sw128(smem + L::kKOff, 16, 1024);
+  const uint64_t dv0 = ptx::desc_sw128(smem + L::kVOff, L::kBlk, 1024);
+
   Cursor cur;
   init_cursor(p, cur, false);
   Unit w;
@@ -413,6 +421,8 @@ __device__ void mma_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint3
     if (!wait_bar(bar(L::QF), q_it & 1u, ctl)) return;
     ptx::tc_fence_after();
     for (int j = 0; j <= nmax; ++j) {
+      // K(j) and V(j-1) are each waited for once per step, by the first user.
+      bool k_ready = false, v_ready = false;
 #pragma unroll
       for (int t = 0; t < kTiles; ++t) {
         const uint32_t tS = tmem + L::kColS + t * 128;
@@ -422,15 +432,18 @@ __device__ void mma_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint3
           ++p_cnt[t];
           const uint32_t it = kv_it + j - 1;
           const uint32_t st = it % NS;
-          if (!wait_bar(bar(L::VF + st), (it / NS) & 1u, ctl)) return;
+          if (!v_ready) {
+            if (!wait_bar(bar(L::VF + st), (it / NS) & 1u, ctl)) return;
+            v_ready = true;
+          }
           ptx::tc_fence_after();
-          const uint32_t vbase = smem + L::kVOff + st * L::kTileBytes;
+          const uint64_t dv = dv0 + ((st * L::kTileBytes) >> 4);
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks) {
             // V is MN-major: 16 keys = 2 swizzle atoms of 8 keys x 128 B;
             // LBO = next 64-column block of D, SBO = next 8 keys.
-            const uint64_t bdesc = ptx::desc_sw128(vbase + ks * 2048, L::kBlk, 1024);
-            ptx::mma_ts(tO, tS + ks * 8, bdesc, kIdPV, (j - 1 > 0 || ks > 0) ? 1u : 0u);
+            ptx::mma_ts(tO, tS + ks * 8, dv + ((ks * 2048) >> 4), kIdPV,
+                        (j - 1 > 0 || ks > 0) ? 1u : 0u);
           }
           if (t == 1 || j - 1 >= w.n[1]) ptx::mma_commit(bar(L::VE + st));
           if (j - 1 == w.n[t] - 1) ptx::mma_commit(bar(L::OF + t));
@@ -438,17 +451,17 @@ __device__ void mma_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint3
         if (j < w.n[t]) {  // S_t(j) = Q_t K(j)^T
           const uint32_t it = kv_it + j;
           const uint32_t st = it % NS;
-          if (!wait_bar(bar(L::KF + st), (it / NS) & 1u, ctl)) return;
-          ptx::tc_fence_after();
-          const uint32_t qbase = smem + L::kQOff + t * L::kTileBytes;
-          const uint32_t kbase = smem + L::kKOff + st * L::kTileBytes;
+          if (!k_ready) {
+            if (!wait_bar(bar(L::KF + st), (it / NS) & 1u, ctl)) return;
+            k_ready = true;
+            ptx::tc_fence_after();
+          }
+          const uint64_t dk = dk0 + ((st * L::kTileBytes) >> 4);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             // K-major, 16 elements = 32 B step inside the 128-B swizzle row.
-            const uint32_t off = (ks >> 2) * L::kBlk + (ks & 3) * 32;
-            const uint64_t adesc = ptx::desc_sw128(qbase + off, 16, 1024);
-            const uint64_t bdesc = ptx::desc_sw128(kbase + off, 16, 1024);
-            ptx::mma_ss(tS, adesc, bdesc, kIdS, ks > 0 ? 1u : 0u);
+            const uint32_t off = ((ks >> 2) * L::kBlk + (ks & 3) * 32) >> 4;
+            ptx::mma_ss(tS, dq[t] + off, dk + off, kIdS, ks > 0 ? 1u : 0u);
           }
           ptx::mma_commit(bar(L::SF + t));
           if (t == 1 || j >= w.n[1]) ptx::mma_commit(bar(L::KE + st));
