@@ -14,15 +14,9 @@
 #include <mutex>
 
 #include "attn.h"
-#include "fwd_kernel.cuh"
+#include "launch.cuh"
 
 namespace attn {
-
-// Instantiated in fwd_d{64,128}_{f16,bf16}.cu
-extern template cudaError_t launch_fwd<64, false>(const FwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_fwd<64, true>(const FwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_fwd<128, false>(const FwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_fwd<128, true>(const FwdParams&, int, cudaStream_t);
 
 namespace {
 
@@ -95,15 +89,15 @@ bool on_device(const void* p, int dev) {
   return a.type == cudaMemoryTypeDevice && a.device == dev;
 }
 
-// [rows, H, D] 16-bit tensor, box = 128 rows x 1 head x 64 elements (128 B),
-// 128-byte swizzle, zero fill outside the tensor.
+// [rows, H, D] 16-bit tensor, box = box_rows rows x 1 head x 64 elements
+// (128 B), 128-byte swizzle, zero fill outside the tensor.
 int encode_rows_heads_dim(CUtensorMap* m, const void* ptr, long long rows, int H, int D,
-                          bool bf16) {
+                          bool bf16, int box_rows = kBM) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                            static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(D) * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBM)};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                         3, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -162,7 +156,8 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   const bool bf16 = dtype == ATTN_DTYPE_BF16;
   if (encode_rows_heads_dim(&p.tm_q, q, rows_q, H, D, bf16) != ATTN_OK ||
       encode_rows_heads_dim(&p.tm_k, k, rows_k, H, D, bf16) != ATTN_OK ||
-      encode_rows_heads_dim(&p.tm_v, v, rows_k, H, D, bf16) != ATTN_OK)
+      encode_rows_heads_dim(&p.tm_v, v, rows_k, H, D, bf16) != ATTN_OK ||
+      encode_rows_heads_dim(&p.tm_kh, k, rows_k, H, D, bf16, kBN / 2) != ATTN_OK)
     return ATTN_ERR_CUDA;
   p.o = o;
   p.lse = lse;
@@ -179,26 +174,15 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   p.scale_pos = scale > 0.0f ? 1 : 0;
   p.timeout_ns = timeout_ns_from_env();
 
-  const long long grid = units_bound < ds->sms ? units_bound : ds->sms;
-  if (grid <= 0) return ATTN_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  int smem;
-  if (D == 64) {
-    smem = Layout<64>::kAlloc;
-    e = bf16 ? launch_fwd<64, true>(p, static_cast<int>(grid), s)
-             : launch_fwd<64, false>(p, static_cast<int>(grid), s);
-  } else {
-    smem = Layout<128>::kAlloc;
-    e = bf16 ? launch_fwd<128, true>(p, static_cast<int>(grid), s)
-             : launch_fwd<128, false>(p, static_cast<int>(grid), s);
-  }
+  LaunchInfo info;
+  const cudaError_t e = launch_forward(p, D, bf16, varlen, B, H, rows_q, Sq, ds->sms, s, &info);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_CUDA;
   }
-  t_last_grid = static_cast<int>(grid);
-  t_last_smem = smem;
+  t_last_grid = info.grid;
+  t_last_smem = info.smem;
   return ATTN_OK;
 }
 

@@ -51,6 +51,7 @@ struct FwdParams {
   CUtensorMap tm_q;          // [rows_q, H, D] 16-bit, box 128 x 1 x 64
   CUtensorMap tm_k;
   CUtensorMap tm_v;
+  CUtensorMap tm_kh;         // K with a 64-row box (pair kernel: each CTA loads half a tile)
   void* o;
   float* lse;
   const int32_t* cu_q;       // varlen only
@@ -131,6 +132,7 @@ struct Cursor {               // forward-only walk over varlen sequences
   int q_start, Lq, k_start, Lk;
 };
 
+template <int UR>
 __device__ __forceinline__ void load_seq(const FwdParams& p, Cursor& c, bool report) {
   c.units = 0;
   c.q_start = c.Lq = c.k_start = c.Lk = 0;
@@ -146,25 +148,28 @@ __device__ __forceinline__ void load_seq(const FwdParams& p, Cursor& c, bool rep
   c.Lq = q1 - q0;
   c.k_start = k0;
   c.Lk = k1 - k0;
-  c.units = p.H * ((c.Lq + kUnitRows - 1) / kUnitRows);
+  c.units = p.H * ((c.Lq + UR - 1) / UR);
 }
 
+template <int UR>
 __device__ __forceinline__ void init_cursor(const FwdParams& p, Cursor& c, bool report) {
   c.b = 0;
   c.base = 0;
-  if (p.varlen) load_seq(p, c, report);
+  if (p.varlen) load_seq<UR>(p, c, report);
 }
 
-// Decodes unit u (units are visited in increasing order by each CTA).
-// Order: (sequence, head) outer, 256-row block inner, heaviest causal blocks
+// Decodes unit u (units are visited in increasing order by each CTA) into its
+// sequence, head and row block of UR query rows.
+// Order: (sequence, head) outer, row block inner, heaviest causal blocks
 // first.  Keeping one head's blocks together keeps the K/V tiles that the
 // concurrently running CTAs stream within L2 (one head of a 64K-token
-// sequence is 32 MB); dealing the units to CTAs in a snake order (next
-// function) keeps the per-CTA work balanced.
-__device__ __forceinline__ bool decode_unit(const FwdParams& p, int u, Cursor& c, Unit& w,
+// sequence is 32 MB); dealing the units to CTAs in a snake order (unit_of)
+// keeps the per-CTA work balanced.
+template <int UR>
+__device__ __forceinline__ bool decode_rows(const FwdParams& p, int u, Cursor& c, Unit& w,
                                             bool report) {
   if (!p.varlen) {
-    const int nU = (p.Sq + kUnitRows - 1) / kUnitRows;
+    const int nU = (p.Sq + UR - 1) / UR;
     if (u >= p.B * p.H * nU) return false;
     const int bh = u / nU;
     const int i = u - bh * nU;
@@ -181,7 +186,7 @@ __device__ __forceinline__ bool decode_unit(const FwdParams& p, int u, Cursor& c
       if (u < c.base + c.units) break;
       c.base += c.units;
       c.b += 1;
-      load_seq(p, c, report);
+      load_seq<UR>(p, c, report);
     }
     const int rem = u - c.base;
     const int nU = c.units / p.H;
@@ -194,24 +199,37 @@ __device__ __forceinline__ bool decode_unit(const FwdParams& p, int u, Cursor& c
     w.k_start = c.k_start;
     w.Lk = c.Lk;
   }
+  return true;
+}
+
+// K/V tiles a 128-row query tile starting at row q0 must visit (0: none).
+__device__ __forceinline__ int tiles_for(const FwdParams& p, const Unit& w, int q0) {
+  if (q0 >= w.Lq) return 0;
   const int nk = (w.Lk + kBN - 1) / kBN;
+  // causal: rows q0..q0+127 see keys <= their index, so tiles up to the diagonal
+  return p.causal ? min(nk, q0 / kBN + 1) : nk;
+}
+
+__device__ __forceinline__ bool decode_unit(const FwdParams& p, int u, Cursor& c, Unit& w,
+                                            bool report) {
+  if (!decode_rows<kUnitRows>(p, u, c, w, report)) return false;
 #pragma unroll
   for (int t = 0; t < kTiles; ++t) {
     const int q0 = w.qt * kUnitRows + t * kBM;
     w.valid[t] = q0 < w.Lq;
-    // causal: rows q0..q0+127 see keys <= their index, so tiles up to the diagonal
-    w.n[t] = !w.valid[t] ? 0 : (p.causal ? min(nk, q0 / kBN + 1) : nk);
+    w.n[t] = tiles_for(p, w, q0);
   }
   return true;
 }
 
-// The k-th unit of this CTA: units are dealt in rounds of gridDim.x, left to
-// right in even rounds and right to left in odd rounds, so that the CTA that
-// got the heaviest unit of one round gets the lightest of the next.
-__device__ __forceinline__ int unit_of(int k) {
-  const int g = static_cast<int>(gridDim.x);
-  const int c = static_cast<int>(blockIdx.x);
+// The k-th unit of worker c out of g: units are dealt in rounds of g, left to
+// right in even rounds and right to left in odd rounds, so that the worker
+// that got the heaviest unit of one round gets the lightest of the next.
+__device__ __forceinline__ int unit_of(int k, int g, int c) {
   return k * g + ((k & 1) ? (g - 1 - c) : c);
+}
+__device__ __forceinline__ int unit_of(int k) {
+  return unit_of(k, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x));
 }
 
 // ---------------------------------------------------------------- softmax
@@ -230,9 +248,13 @@ struct RowState {
 // the first 64 columns of S.  O is rescaled in TMEM when the running max moved
 // by more than 2^kRescaleLog2; otherwise the stale max is kept for P and l,
 // which leaves the result exact.
+// pvd_bar != 0: before rescaling O, wait (parity pvd_parity) for the MMA that
+// accumulates the previous tile into O; returns false if that wait gave up.
 template <int D, bool BF16>
-__device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, int limit, float cl,
-                                             bool scale_pos, bool first, RowState& st) {
+__device__ __forceinline__ bool softmax_step_pv(uint32_t tS, uint32_t tO, int limit, float cl,
+                                                bool scale_pos, bool first, RowState& st,
+                                                uint32_t pvd_bar, uint32_t pvd_parity,
+                                                const Ctl& ctl) {
   uint32_t r[128];
   ptx::tmem_ld_x128(tS, r);
   float cle = cl;
@@ -299,6 +321,10 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, int limit
   st.l_p = st.l_p * alpha + ((lp0 + lp1) + (lp2 + lp3));
 
   if (!first && __any_sync(0xffffffffu, rescale)) {
+    if (pvd_bar != 0) {
+      if (!wait_bar_warp(pvd_bar, pvd_parity, ctl)) return false;
+      ptx::tc_fence_after();
+    }
     const uint64_t al2 = ptx::f2(alpha, alpha);
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
@@ -316,6 +342,7 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, int limit
     }
   }
   ptx::tmem_wait_st();
+  return true;
 }
 
 template <int D, bool BF16>
@@ -337,7 +364,7 @@ __device__ void softmax_role(const FwdParams& p, int t, uint32_t tmem, uint32_t 
   out_t* const O = static_cast<out_t*>(p.o);
 
   Cursor cur;
-  init_cursor(p, cur, false);
+  init_cursor<kUnitRows>(p, cur, false);
   Unit w;
   for (int k = 0; decode_unit(p, unit_of(k), cur, w, false); ++k) {
     if (!(t == 0 ? w.valid[0] : w.valid[1])) continue;
@@ -358,7 +385,9 @@ __device__ void softmax_role(const FwdParams& p, int t, uint32_t tmem, uint32_t 
         ptx::tc_fence_after();
         int limit = (p.causal && j == diag) ? row : 127;
         limit = min(limit, w.Lk - j * kBN - 1);
-        softmax_step<D, BF16>(tS, tO, limit, p.scale_log2, p.scale_pos != 0, j == 0, rs);
+        // the S(j) commit implies O += P(j-1) V(j-1) is done: no extra wait
+        softmax_step_pv<D, BF16>(tS, tO, limit, p.scale_log2, p.scale_pos != 0, j == 0, rs, 0u,
+                                 0u, ctl);
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar_p);
       }
@@ -413,7 +442,7 @@ __device__ void mma_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint3
   const uint64_t dv0 = ptx::desc_sw128(smem + L::kVOff, L::kBlk, 1024);
 
   Cursor cur;
-  init_cursor(p, cur, false);
+  init_cursor<kUnitRows>(p, cur, false);
   Unit w;
   for (int k = 0; decode_unit(p, unit_of(k), cur, w, false); ++k) {
     const int nmax = max(w.n[0], w.n[1]);
@@ -494,7 +523,7 @@ __device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bars, cons
   constexpr int NS = L::kStages;
   auto bar = [&](int i) { return bars + 8u * i; };
   Cursor cur;
-  init_cursor(p, cur, true);
+  init_cursor<kUnitRows>(p, cur, true);
   Unit w;
   for (int k = 0; decode_unit(p, unit_of(k), cur, w, true); ++k) {
     const int nmax = max(w.n[0], w.n[1]);

@@ -1,0 +1,415 @@
+// Fused attention forward, head dim 128, on CTA pairs (clusters of 2) with
+// 2-SM tcgen05 MMAs and a triple-buffered score tile.
+//
+// Same computation as attn_fwd_kernel (see fwd_kernel.cuh for the definition
+// and its sources).  What changes is how the tensor cores are fed:
+//   * One M = 256 tcgen05.mma (cta_group::2), issued by the even CTA of the
+//     pair, covers 128 query rows of each CTA.  Each CTA reads only half of
+//     every K/V tile from shared memory (K: 64 of the 128 keys; V: 64 of the
+//     128 head-dim columns) and loads only that half with TMA.
+//   * Each CTA owns one 128-row query tile and three S buffers in tensor
+//     memory, so S(G+1) and S(G+2) = Q K^T are ready while the softmax works
+//     on S(G): the only ordering left is P(G) -> O += P(G) V(G) -> S(G+3)
+//     (P(G) is written over S(G), so S(G+3) reuses that buffer once P(G) has
+//     been consumed).  With two buffers the softmax waited for that chain.
+//   * TMEM per CTA: S buffers 0, 1, 2 | O (128 columns each, all 512 used).
+//   * Two threads of the even CTA issue the MMAs: one the S = Q K^T products,
+//     one the O += P V products.  A single issuing thread was the bottleneck
+//     (each barrier poll and each 2-SM MMA issue costs it tens to hundreds of
+//     cycles), and the two streams only meet at "PV done": S(G) may overwrite
+//     the buffer of P(G-3) once O += P(G-3) V(G-3) has completed.
+// Steps are numbered globally per pair (G = steps of earlier units + j), so
+// buffer G % 3 and the phase of every per-step barrier carry across units.
+// Work unit = (sequence, head, 256 query rows): CTA r of the pair holds rows
+// 256u + 128r .. +127.  Both CTAs' softmax warps run every K/V step of the pair
+// (masking what their own rows cannot see) and signal the even CTA, whose two
+// MMA threads issue all MMAs.  Barriers: Q/K/V "full" and "P ready"
+// live in the even CTA (the odd CTA's copies complete their bytes there, its
+// softmax warps arrive there); "S ready", "PV done", "O ready" and the "empty"
+// barriers are multicast to both CTAs.
+#pragma once
+
+#include "fwd_kernel.cuh"
+
+namespace attn {
+namespace pair {
+
+constexpr int D = 128;
+constexpr int kUR = 2 * kBM;    // query rows per pair unit
+constexpr int kStages = 5;      // K/V ring depth (half tiles: 16 KiB each)
+constexpr int kNBuf = 3;        // S buffers in tensor memory
+constexpr int kWarps = 7;       // 4 softmax warps, S-MMA warp, load warp, PV-MMA warp
+constexpr int kPairThreads = kWarps * 32;
+constexpr int kPMma = 4;        // issues S = Q K^T; allocates tensor memory
+constexpr int kPLoad = 5;
+constexpr int kPPv = 6;         // issues O += P V
+
+struct Layout {
+  static constexpr int kBlk = 16384;
+  static constexpr int kQTile = 2 * kBlk;          // 128 rows x 128 dims
+  static constexpr int kKHalf = 16384;             // 64 keys x 128 dims (two 8 KiB blocks)
+  static constexpr int kKBlk = 8192;
+  static constexpr int kVHalf = 16384;             // 128 keys x 64 dims (one block)
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kQTile;
+  static constexpr int kVOff = kKOff + kStages * kKHalf;
+  static constexpr int kBarOff = kVOff + kStages * kVHalf;
+  static constexpr int QF = 0, QE = 1, KF = 2, KE = KF + kStages, VF = KE + kStages,
+                       VE = VF + kStages, SF = VE + kStages, PF = SF + kNBuf,
+                       PVD = PF + kNBuf, OF = PVD + kNBuf, DONE = OF + 1, kNumBars = DONE + 1;
+  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  static constexpr uint32_t kColS = 0, kColO = kNBuf * 128;
+  // Per-step barriers come in threes indexed by G % 3; barrier G % 3 completes
+  // its phase G / 3 for step G.  No barrier can run two phases ahead of a
+  // waiter:
+  //   S ready (SF):  S(G+3) needs O += P(G) V(G), which needs the softmax to
+  //                  have consumed S(G);
+  //   P ready (PF):  a softmax warp can be two steps ahead of the others
+  //                  (S(G+1), S(G+2) may be computed), never three (S(G+3)
+  //                  needs every warp's P(G));
+  //   PV done (PVD): PV(G+3) needs S(G+3), which the S thread issues only after
+  //                  waiting for PV(G); the softmax waits for PV(G-1) before
+  //                  giving P(G), which PV(G+2) needs.
+  static constexpr uint32_t kPArrivals = 2 * 4;  // one per softmax warp of each CTA
+  static constexpr uint32_t kDoneArrivals = 2;   // both MMA threads
+};
+
+// Same as wait_bar, but with cluster-scope acquire (used where the peer CTA arrives).
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, const Ctl& c) {
+  if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = ptx::global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+    if ((n & 15u) == 0) {
+      if (*c.abort_flag) return false;
+      if (static_cast<long long>(ptx::global_timer_ns() - t0) > c.timeout_ns) {
+        *c.abort_flag = 1;
+        atomicOr(c.err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ int q0_of(const Unit& w, int r) { return w.qt * kUR + r * kBM; }
+
+// Decodes the k-th unit of this pair; n = K/V steps of the pair (max over the
+// two CTAs' query tiles).
+__device__ __forceinline__ bool decode_pair(const FwdParams& p, int k, Cursor& c, Unit& w,
+                                            int& n, bool report) {
+  const int g = static_cast<int>(gridDim.x) / 2;
+  const int cl = static_cast<int>(blockIdx.x) / 2;
+  if (!decode_rows<kUR>(p, unit_of(k, g, cl), c, w, report)) return false;
+  n = max(tiles_for(p, w, q0_of(w, 0)), tiles_for(p, w, q0_of(w, 1)));
+  return true;
+}
+
+// ---------------------------------------------------------------- softmax
+template <bool BF16>
+__device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, uint32_t bars,
+                             const Ctl& ctl) {
+  using L = Layout;
+  const int warp = threadIdx.x >> 5;  // 0..3
+  const int lane = threadIdx.x & 31;
+  const int row = warp * 32 + lane;
+  const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tO = tmem + lane_bits + L::kColO;
+  const uint32_t bar_p_lead = ptx::mapa(bars + 8 * L::PF, 0);  // + 8 * (G % 3)
+  const uint32_t bar_o = bars + 8 * L::OF;
+  uint32_t o_cnt = 0, g_base = 0;
+  uint16_t* const O = static_cast<uint16_t*>(p.o);
+
+  Cursor cur;
+  init_cursor<kUR>(p, cur, false);
+  Unit w;
+  int n = 0;
+  for (int k = 0; decode_pair(p, k, cur, w, n, false); ++k) {
+    const int q0 = q0_of(w, static_cast<int>(rank));
+    if (q0 >= w.Lq && n == 0) continue;
+    const int qrow = q0 + row;
+    const bool row_ok = qrow < w.Lq;
+    const long long orow = (static_cast<long long>(w.q_start) + qrow) * p.H + w.h;
+    const long long lidx = p.varlen
+                               ? static_cast<long long>(w.h) * p.Sq + w.q_start + qrow
+                               : (static_cast<long long>(w.b) * p.H + w.h) * p.Sq + qrow;
+    RowState rs{-INFINITY, 0.0f, 0.0f};
+    if (n > 0) {
+      for (int j = 0; j < n; ++j) {
+        const uint32_t G = g_base + j;
+        const uint32_t b = G % kNBuf;
+        if (!wait_bar_warp(bars + 8 * (L::SF + b), (G / kNBuf) & 1u, ctl)) return;
+        ptx::tc_fence_after();
+        int limit = p.causal ? min(127, qrow - j * kBN) : 127;
+        limit = min(limit, w.Lk - j * kBN - 1);
+        // O += P(G-1) V(G-1) may still be running: a rescale of O waits for it.
+        const uint32_t gp = G - 1;
+        if (!softmax_step_pv<D, BF16>(tmem + lane_bits + L::kColS + b * 128, tO, limit,
+                                      p.scale_log2, p.scale_pos != 0, j == 0, rs,
+                                      bars + 8 * (L::PVD + gp % kNBuf), (gp / kNBuf) & 1u,
+                                      ctl))
+          return;
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster_relaxed(bar_p_lead + 8u * b);
+      }
+      g_base += n;
+      if (!wait_bar_warp(bar_o, o_cnt & 1u, ctl)) return;
+      ++o_cnt;
+      ptx::tc_fence_after();
+      const float inv_l = rs.l_p > 0.0f ? 1.0f / rs.l_p : 0.0f;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        ptx::tmem_ld_x32(tO + c0, o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = ptx::pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
+                                   __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(O + orow * D + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+    } else if (row_ok) {  // no visible key at all: O = 0, LSE = -inf
+      uint4* dst = reinterpret_cast<uint4*>(O + orow * D);
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (row_ok) {
+      p.lse[lidx] = rs.l_x > 0.0f ? (rs.m + ptx::lg2(rs.l_x)) * 0.69314718055994531f : -INFINITY;
+    }
+  }
+}
+
+// -------------------------------------------------------------------- MMA
+// S thread: lane 0 of warp kPMma of the even CTA.
+template <bool BF16>
+__device__ void s_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint32_t bars,
+                       const Ctl& ctl) {
+  using L = Layout;
+  constexpr int NS = kStages;
+  constexpr uint32_t kIdS = ptx::idesc_f16_f32acc(BF16, 2 * kBM, kBN, false);
+  constexpr uint16_t kBoth = 3;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  uint32_t g_base = 0, q_it = 0;
+  const uint64_t dq = ptx::desc_sw128(smem + L::kQOff, 16, 1024);
+  const uint64_t dk0 = ptx::desc_sw128(smem + L::kKOff, 16, 1024);
+  Cursor cur;
+  init_cursor<kUR>(p, cur, false);
+  Unit w;
+  int n = 0;
+  for (int k = 0; decode_pair(p, k, cur, w, n, false); ++k) {
+    if (n == 0) continue;
+    if (!wait_bar(bar(L::QF), q_it & 1u, ctl)) return;
+    ptx::tc_fence_after();
+    for (int j = 0; j < n; ++j) {
+      const uint32_t G = g_base + j;
+      if (G >= kNBuf) {  // buffer G % 3 holds P(G-3) until O += P(G-3) V(G-3) is done
+        const uint32_t gp = G - kNBuf;
+        if (!wait_bar(bar(L::PVD + gp % kNBuf), (gp / kNBuf) & 1u, ctl)) return;
+      }
+      const uint32_t st = G % NS;
+      if (!wait_bar(bar(L::KF + st), (G / NS) & 1u, ctl)) return;
+      ptx::tc_fence_after();
+      const uint64_t dk = dk0 + ((st * L::kKHalf) >> 4);
+      const uint32_t tS = tmem + L::kColS + (G % kNBuf) * 128;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t qoff = ((ks >> 2) * L::kBlk + (ks & 3) * 32) >> 4;
+        const uint32_t koff = ((ks >> 2) * L::kKBlk + (ks & 3) * 32) >> 4;
+        ptx::mma_ss_pair(tS, dq + qoff, dk + koff, kIdS, ks > 0 ? 1u : 0u);
+      }
+      ptx::mma_commit_pair(bar(L::SF + G % kNBuf), kBoth);
+      ptx::mma_commit_pair(bar(L::KE + st), kBoth);
+      if (j == n - 1) ptx::mma_commit_pair(bar(L::QE), kBoth);  // Q no longer read
+    }
+    g_base += n;
+    ++q_it;
+  }
+}
+
+// PV thread: lane 0 of warp kPPv of the even CTA.
+template <bool BF16>
+__device__ void pv_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint32_t bars,
+                        const Ctl& ctl) {
+  using L = Layout;
+  constexpr int NS = kStages;
+  constexpr uint32_t kIdPV = ptx::idesc_f16_f32acc(BF16, 2 * kBM, D, true);
+  constexpr uint16_t kBoth = 3;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  uint32_t g_base = 0;
+  const uint64_t dv0 = ptx::desc_sw128(smem + L::kVOff, L::kBlk, 1024);
+  const uint32_t tO = tmem + L::kColO;
+  Cursor cur;
+  init_cursor<kUR>(p, cur, false);
+  Unit w;
+  int n = 0;
+  for (int k = 0; decode_pair(p, k, cur, w, n, false); ++k) {
+    if (n == 0) continue;
+    for (int j = 0; j < n; ++j) {
+      const uint32_t G = g_base + j;
+      // O += P(G) V(G): P(G) in buffer G % 3 of both CTAs
+      if (!wait_bar_cluster(bar(L::PF + G % kNBuf), (G / kNBuf) & 1u, ctl)) return;
+      const uint32_t st = G % NS;
+      if (!wait_bar(bar(L::VF + st), (G / NS) & 1u, ctl)) return;
+      ptx::tc_fence_after();
+      const uint64_t dv = dv0 + ((st * L::kVHalf) >> 4);
+      const uint32_t tP = tmem + L::kColS + (G % kNBuf) * 128;
+#pragma unroll
+      for (int ks = 0; ks < kBN / 16; ++ks)
+        ptx::mma_ts_pair(tO, tP + ks * 8, dv + ((ks * 2048) >> 4), kIdPV,
+                         (j > 0 || ks > 0) ? 1u : 0u);
+      ptx::mma_commit_pair(bar(L::VE + st), kBoth);
+      ptx::mma_commit_pair(bar(L::PVD + G % kNBuf), kBoth);
+      if (j == n - 1) ptx::mma_commit_pair(bar(L::OF), kBoth);
+    }
+    g_base += n;
+  }
+}
+
+// Each MMA thread makes sure its own tcgen05 operations retired before TMEM is
+// freed, also when its loop was abandoned.
+__device__ __forceinline__ void mma_drain(uint32_t bars, const Ctl& ctl) {
+  const uint32_t done = bars + 8u * Layout::DONE;
+  ptx::mma_commit_pair(done, 1);
+  wait_bar(done, 0, ctl, false);
+}
+
+// ------------------------------------------------------------------- load
+// Runs on lane 0 of the load warp of both CTAs; each loads its own Q tile and
+// its half of every K/V tile, counting the bytes on the even CTA's barriers.
+static __device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bars, uint32_t rank,
+                                 const Ctl& ctl, uint32_t& kv_it, uint32_t& q_it) {
+  using L = Layout;
+  constexpr int NS = kStages;
+  const bool lead = rank == 0;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  auto lbar = [&](int i) { return ptx::mapa(bars + 8u * i, 0); };
+  Cursor cur;
+  init_cursor<kUR>(p, cur, true);
+  Unit w;
+  int n = 0;
+  for (int k = 0; decode_pair(p, k, cur, w, n, lead); ++k) {
+    if (n == 0) continue;
+    if (q_it > 0 && !wait_bar(bar(L::QE), (q_it - 1) & 1u, ctl)) return;
+    if (lead) ptx::mbar_arrive_expect_tx(bar(L::QF), 2 * L::kQTile);
+#pragma unroll
+    for (int blk = 0; blk < D / 64; ++blk)
+      ptx::tma_load_3d_pair(smem + L::kQOff + blk * L::kBlk, &p.tm_q, lbar(L::QF), blk * 64, w.h,
+                            w.q_start + q0_of(w, static_cast<int>(rank)));
+    ++q_it;
+    for (int j = 0; j < n; ++j) {
+      const uint32_t it = kv_it + j;
+      const uint32_t st = it % NS;
+      const int krow = w.k_start + j * kBN;
+      if (it >= NS && !wait_bar(bar(L::KE + st), (it / NS - 1) & 1u, ctl)) return;
+      if (lead) ptx::mbar_arrive_expect_tx(bar(L::KF + st), 2 * L::kKHalf);
+#pragma unroll
+      for (int blk = 0; blk < D / 64; ++blk)
+        ptx::tma_load_3d_pair(smem + L::kKOff + st * L::kKHalf + blk * L::kKBlk, &p.tm_kh,
+                              lbar(L::KF + st), blk * 64, w.h, krow + 64 * static_cast<int>(rank));
+      if (it >= NS && !wait_bar(bar(L::VE + st), (it / NS - 1) & 1u, ctl)) return;
+      if (lead) ptx::mbar_arrive_expect_tx(bar(L::VF + st), 2 * L::kVHalf);
+      ptx::tma_load_3d_pair(smem + L::kVOff + st * L::kVHalf, &p.tm_v, lbar(L::VF + st),
+                            64 * static_cast<int>(rank), w.h, krow);
+    }
+    kv_it += n;
+  }
+}
+
+static __device__ void load_role(const FwdParams& p, uint32_t smem, uint32_t bars, uint32_t rank,
+                                 const Ctl& ctl) {
+  using L = Layout;
+  uint32_t kv_it = 0, q_it = 0;
+  load_loop(p, smem, bars, rank, ctl, kv_it, q_it);
+  if (rank != 0) return;
+  // The even CTA's "full" barriers count both CTAs' copies: waiting for the
+  // last phase of each means no copy of the pair is still in flight.
+  if (q_it > 0) wait_bar(bars + 8u * L::QF, (q_it - 1) & 1u, ctl, false);
+  for (uint32_t st = 0; st < static_cast<uint32_t>(kStages) && st < kv_it; ++st) {
+    const uint32_t last = st + ((kv_it - 1 - st) / kStages) * kStages;
+    wait_bar(bars + 8u * (L::KF + st), (last / kStages) & 1u, ctl, false);
+    wait_bar(bars + 8u * (L::VF + st), (last / kStages) & 1u, ctl, false);
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <bool BF16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+    attn_fwd_kernel_2sm(const __grid_constant__ FwdParams p) {
+  using L = Layout;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t smem = (raw + 1023u) & ~1023u;
+  uint8_t* const base = smem_raw + (smem - raw);
+  const uint32_t bars = smem + L::kBarOff;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base + L::kMiscOff);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(base + L::kMiscOff + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_rank();
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::kNumBars; ++i)
+      ptx::mbar_init(bars + 8u * i, (i >= L::PF && i < L::PF + kNBuf) ? L::kPArrivals
+                                    : i == L::DONE                  ? L::kDoneArrivals
+                                                                    : 1u);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA use
+  if (warp == kPMma) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  if (warp == kPLoad && lane == 0) {
+    ptx::tma_prefetch_desc(&p.tm_q);
+    ptx::tma_prefetch_desc(&p.tm_kh);
+    ptx::tma_prefetch_desc(&p.tm_v);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Ctl ctl{abort_flag, p.err, p.timeout_ns};
+
+  if (warp < kPMma) {
+    softmax_role<BF16>(p, rank, tmem, bars, ctl);
+  } else if (warp == kPMma) {
+    if (lane == 0 && rank == 0) {
+      s_loop<BF16>(p, smem, tmem, bars, ctl);
+      mma_drain(bars, ctl);
+    }
+  } else if (warp == kPPv) {
+    if (lane == 0 && rank == 0) {
+      pv_loop<BF16>(p, smem, tmem, bars, ctl);
+      mma_drain(bars, ctl);
+    }
+  } else if (lane == 0) {
+    load_role(p, smem, bars, rank, ctl);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // the even CTA's MMAs (reading both CTAs) are all retired
+  ptx::tc_fence_after();
+  if (warp == kPMma) ptx::tmem_dealloc_pair(tmem, kTmemCols);
+}
+
+template <bool BF16>
+cudaError_t launch_fwd_2sm(const FwdParams& p, int grid, cudaStream_t stream) {
+  const void* fn = reinterpret_cast<const void*>(&attn_fwd_kernel_2sm<BF16>);
+  cudaError_t e =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout::kAlloc);
+  if (e != cudaSuccess) return e;
+  void* args[] = {const_cast<FwdParams*>(&p)};
+  return cudaLaunchKernel(fn, dim3(grid), dim3(kPairThreads), args, Layout::kAlloc, stream);
+}
+
+}  // namespace pair
+}  // namespace attn

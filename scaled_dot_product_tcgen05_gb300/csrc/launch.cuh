@@ -1,0 +1,64 @@
+// Host-side kernel choice and launch shared by the C entry points.
+#pragma once
+
+#include <cstdlib>
+
+#include "fwd_kernel.cuh"
+#include "fwd_kernel_2sm.cuh"
+
+namespace attn {
+
+extern template cudaError_t launch_fwd<64, false>(const FwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_fwd<64, true>(const FwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_fwd<128, false>(const FwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_fwd<128, true>(const FwdParams&, int, cudaStream_t);
+namespace pair {
+extern template cudaError_t launch_fwd_2sm<false>(const FwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_fwd_2sm<true>(const FwdParams&, int, cudaStream_t);
+}  // namespace pair
+
+struct LaunchInfo {
+  int grid = 0;
+  int smem = 0;
+  bool pair = false;
+};
+
+// Upper bound of the work units of a call with `rows_per_unit` query rows per unit.
+inline long long units_bound(bool varlen, int B, int H, long long rows_q, int Sq,
+                             int rows_per_unit) {
+  return varlen ? static_cast<long long>(H) * ((rows_q + rows_per_unit - 1) / rows_per_unit + B)
+                : static_cast<long long>(B) * H * ((Sq + rows_per_unit - 1) / rows_per_unit);
+}
+
+// The single-CTA kernel runs by default.  ATTN_PAIR=1 selects the CTA-pair
+// kernel (2-SM MMAs) for head dim 128.  The grid is persistent: at most one
+// CTA per SM.
+inline cudaError_t launch_forward(const FwdParams& p, int D, bool bf16, bool varlen, int B, int H,
+                                  long long rows_q, int Sq, int sms, cudaStream_t s,
+                                  LaunchInfo* info) {
+  const char* sel = std::getenv("ATTN_PAIR");
+  const bool use_pair = D == 128 && sms >= 2 && sel != nullptr && sel[0] == '1';
+  if (use_pair) {
+    const long long units = units_bound(varlen, B, H, rows_q, Sq, pair::kUR);
+    const long long pairs = units < sms / 2 ? units : sms / 2;
+    info->grid = static_cast<int>(2 * pairs);
+    info->smem = pair::Layout::kAlloc;
+    info->pair = true;
+    if (pairs <= 0) return cudaSuccess;
+    return bf16 ? pair::launch_fwd_2sm<true>(p, info->grid, s)
+                : pair::launch_fwd_2sm<false>(p, info->grid, s);
+  }
+  const long long units = units_bound(varlen, B, H, rows_q, Sq, kUnitRows);
+  info->grid = static_cast<int>(units < sms ? units : sms);
+  info->pair = false;
+  if (D == 64) {
+    info->smem = Layout<64>::kAlloc;
+    if (info->grid <= 0) return cudaSuccess;
+    return bf16 ? launch_fwd<64, true>(p, info->grid, s) : launch_fwd<64, false>(p, info->grid, s);
+  }
+  info->smem = Layout<128>::kAlloc;
+  if (info->grid <= 0) return cudaSuccess;
+  return bf16 ? launch_fwd<128, true>(p, info->grid, s) : launch_fwd<128, false>(p, info->grid, s);
+}
+
+}  // namespace attn

@@ -35,14 +35,9 @@
 #include <mutex>
 
 #include "attn.h"
-#include "fwd_kernel.cuh"
+#include "launch.cuh"
 
 namespace attn {
-
-extern template cudaError_t launch_fwd<64, false>(const FwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_fwd<64, true>(const FwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_fwd<128, false>(const FwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_fwd<128, true>(const FwdParams&, int, cudaStream_t);
 
 namespace {
 
@@ -117,12 +112,13 @@ bool na_on_device(const void* p, int dev) {
   return a.type == cudaMemoryTypeDevice && a.device == dev;
 }
 
-int na_encode(CUtensorMap* m, const void* ptr, long long rows, int H, int D, bool bf16) {
+int na_encode(CUtensorMap* m, const void* ptr, long long rows, int H, int D, bool bf16,
+              int box_rows = kBM) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                            static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(D) * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBM)};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_na_encode(
       m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
@@ -186,7 +182,8 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   const bool bf16 = dtype == ATTN_DTYPE_BF16;
   if (na_encode(&p.tm_q, q, rows_q, H, D, bf16) != ATTN_OK ||
       na_encode(&p.tm_k, k, rows_k, H, D, bf16) != ATTN_OK ||
-      na_encode(&p.tm_v, v, rows_k, H, D, bf16) != ATTN_OK)
+      na_encode(&p.tm_v, v, rows_k, H, D, bf16) != ATTN_OK ||
+      na_encode(&p.tm_kh, k, rows_k, H, D, bf16, kBN / 2) != ATTN_OK)
     return ATTN_ERR_CUDA;
   p.o = o;
   p.lse = lse;
@@ -203,22 +200,14 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   p.scale_pos = scale > 0.0f ? 1 : 0;
   p.timeout_ns = 5000LL * 1000000LL;
 
-  const long long grid = units_bound < ds->sms ? units_bound : ds->sms;
-  if (grid <= 0) return ATTN_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the shared error word must start at zero for this call
   if (cudaMemsetAsync(ds->scratch, 0, sizeof(int), s) != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_CUDA;
   }
-  cudaError_t e;
-  if (D == 64) {
-    e = bf16 ? launch_fwd<64, true>(p, static_cast<int>(grid), s)
-             : launch_fwd<64, false>(p, static_cast<int>(grid), s);
-  } else {
-    e = bf16 ? launch_fwd<128, true>(p, static_cast<int>(grid), s)
-             : launch_fwd<128, false>(p, static_cast<int>(grid), s);
-  }
+  LaunchInfo info;
+  const cudaError_t e = launch_forward(p, D, bf16, varlen, B, H, rows_q, Sq, ds->sms, s, &info);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_CUDA;

@@ -190,3 +190,38 @@ def test_grid_is_persistent():
     run_gpu(q, k, v, True, 0.088)
     grid, smem = pkg.last_launch()
     assert grid == pkg.num_sms() and smem <= 232448
+
+
+PAIR_CASES = [
+    (2, 3, 700, 700, torch.bfloat16, True),
+    (1, 2, 300, 520, torch.float16, False),
+    (1, 4, 2050, 2050, torch.bfloat16, True),
+    (2, 2, 77, 300, torch.float16, True),
+]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: "B{}H{}q{}k{}{}{}".format(
+    c[0], c[1], c[2], c[3], "bf" if c[4] == torch.bfloat16 else "fp", "c" if c[5] else ""))
+def test_cta_pair_kernel(case, monkeypatch):
+    """Head dim 128 on CTA pairs (2-SM MMAs), selected with ATTN_PAIR=1."""
+    monkeypatch.setenv("ATTN_PAIR", "1")
+    B, H, Sq, Sk, dt, causal = case
+    q, k, v = _dense_case(Sq + 5 * Sk, B, H, Sq, Sk, 128, dt)
+    o, lse = run_gpu(q, k, v, causal, 1 / math.sqrt(128))
+    grid, _ = pkg.last_launch()
+    assert grid % 2 == 0
+    o_ref, l_ref = attention_dense(q, k, v, 1 / math.sqrt(128), causal)
+    compare(o, lse, o_ref, l_ref, what=f"pair {case}")
+
+
+def test_cta_pair_kernel_varlen(monkeypatch):
+    monkeypatch.setenv("ATTN_PAIR", "1")
+    for causal in (False, True):
+        lens_q = [1, 0, 300, 129, 5, 256, 1000]
+        lens_k = [1, 7, 300, 129, 0, 100, 1000]
+        q, k, v, cq, ck = _varlen(14, lens_q, lens_k, 3, 128, torch.bfloat16)
+        o, lse = run_gpu(q, k, v, causal, 0.09, cq, ck)
+        o_ref, l_ref = attention_varlen(q, k, v, cq, ck, 0.09, causal)
+        compare(o, lse, o_ref, l_ref, what=f"pair varlen causal={causal}")
+        a, b = int(cq[4]), int(cq[5])
+        assert torch.all(o[a:b] == 0) and torch.all(torch.isneginf(lse[:, a:b]))
