@@ -38,11 +38,12 @@ constexpr int D = 128;
 constexpr int kUR = 2 * kBM;    // query rows per pair unit
 constexpr int kStages = 5;      // K/V ring depth (half tiles: 16 KiB each)
 constexpr int kNBuf = 3;        // S buffers in tensor memory
-constexpr int kWarps = 7;       // 4 softmax warps, S-MMA warp, load warp, PV-MMA warp
+constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quarter: column halves 0 and 1
+constexpr int kWarps = kSoftmaxWarps + 3;  // + S-MMA warp, load warp, PV-MMA warp
 constexpr int kPairThreads = kWarps * 32;
-constexpr int kPMma = 4;        // issues S = Q K^T; allocates tensor memory
-constexpr int kPLoad = 5;
-constexpr int kPPv = 6;         // issues O += P V
+constexpr int kPMma = 8;        // issues S = Q K^T; allocates tensor memory
+constexpr int kPLoad = 9;
+constexpr int kPPv = 10;        // issues O += P V
 
 struct Layout {
   static constexpr int kBlk = 16384;
@@ -58,7 +59,11 @@ struct Layout {
                        VE = VF + kStages, SF = VE + kStages, PF = SF + kNBuf,
                        PVD = PF + kNBuf, OF = PVD + kNBuf, DONE = OF + 1, kNumBars = DONE + 1;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
-  static constexpr int kBytes = kMiscOff + 16;
+  // softmax exchange between the two warps of a row: per-step partial maxima
+  // (two step parities x two halves x 128 rows) and the final row sums
+  static constexpr int kXMaxOff = kMiscOff + 16;
+  static constexpr int kXSumOff = kXMaxOff + 2 * 2 * 128 * 4;
+  static constexpr int kBytes = kXSumOff + 2 * 128 * 2 * 4;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t kColS = 0, kColO = kNBuf * 128;
   // Per-step barriers come in threes indexed by G % 3; barrier G % 3 completes
@@ -72,7 +77,7 @@ struct Layout {
   //   PV done (PVD): PV(G+3) needs S(G+3), which the S thread issues only after
   //                  waiting for PV(G); the softmax waits for PV(G-1) before
   //                  giving P(G), which PV(G+2) needs.
-  static constexpr uint32_t kPArrivals = 2 * 4;  // one per softmax warp of each CTA
+  static constexpr uint32_t kPArrivals = 2 * kSoftmaxWarps;  // every softmax warp, both CTAs
   static constexpr uint32_t kDoneArrivals = 2;   // both MMA threads
 };
 
@@ -107,17 +112,125 @@ __device__ __forceinline__ bool decode_pair(const FwdParams& p, int k, Cursor& c
 }
 
 // ---------------------------------------------------------------- softmax
+// One K/V step of the online softmax for half of a query row: this thread owns
+// keys [64h, 64h+64) of S (the other half sits with the thread of the same lane
+// in warp w ^ 4, on the same SM sub-partition and TMEM lane quarter).  The two
+// halves exchange their partial maxima through shared memory at a named
+// barrier, so both take the same running max and rescale decisions; each
+// writes its 32 columns of P and rescales its 64 columns of O.  Masking: keys
+// c of this half with c > limit are invisible (limit already local to the half).
+template <bool BF16>
+__device__ __forceinline__ bool softmax_half_step(uint32_t tS, uint32_t tP, uint32_t tO, int limit,
+                                                  float cl, bool scale_pos, bool first,
+                                                  RowState& st, float* x_mine,
+                                                  const float* x_other, uint32_t bar_id,
+                                                  uint32_t pvd_bar, uint32_t pvd_parity,
+                                                  const Ctl& ctl) {
+  uint32_t r[64];
+  ptx::tmem_ld_x64(tS, r);
+  float cle = cl;
+  if (!scale_pos) {  // scale <= 0: scale first so that "max" stays a max
+#pragma unroll
+    for (int c = 0; c < 64; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * cl);
+    cle = 1.0f;
+  }
+  if (limit < 63) {
+#pragma unroll
+    for (int c = 0; c < 64; ++c)
+      if (c > limit) r[c] = __float_as_uint(-INFINITY);
+  }
+  float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 64; c += 8) {
+    mx0 = ptx::max3(mx0, __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+    mx1 = ptx::max3(mx1, __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]));
+    mx2 = ptx::max3(mx2, __uint_as_float(r[c + 4]), __uint_as_float(r[c + 5]));
+    mx3 = ptx::max3(mx3, __uint_as_float(r[c + 6]), __uint_as_float(r[c + 7]));
+  }
+  const float m_part = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cle;
+  *x_mine = m_part;
+  // Both halves have read their S columns (tcgen05.ld waited) before either
+  // overwrites the first 64 columns of the buffer with P.
+  ptx::tc_fence_before();
+  ptx::named_bar_sync(bar_id, 64);
+  ptx::tc_fence_after();
+  const float m_tile = fmaxf(m_part, *x_other);
+  const float m_new = fmaxf(st.m, m_tile);
+  const bool rescale = m_new > st.m + kRescaleLog2;  // always true on the first tile
+  const float m_use = rescale ? m_new : st.m;
+  const float m_safe = (m_use == -INFINITY) ? 0.0f : m_use;
+  const float alpha = rescale ? ptx::ex2(st.m - m_safe) : 1.0f;
+  st.m = m_use;
+
+  const uint64_t cl2 = ptx::f2(cle, cle);
+  const uint64_t nm2 = ptx::f2(-m_safe, -m_safe);
+  uint64_t lx0 = ptx::f2(0.f, 0.f), lx1 = lx0;
+  float lp0 = 0.f, lp1 = 0.f, lp2 = 0.f, lp3 = 0.f;
+  uint32_t pk[32];
+#pragma unroll
+  for (int c = 0; c < 64; c += 4) {
+    float x0, x1, x2, x3;
+    ptx::f2_split(ptx::f2_fma(ptx::f2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), cl2,
+                              nm2), x0, x1);
+    ptx::f2_split(ptx::f2_fma(ptx::f2(__uint_as_float(r[c + 2]), __uint_as_float(r[c + 3])),
+                              cl2, nm2), x2, x3);
+    const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1), p2 = ptx::ex2(x2), p3 = ptx::ex2(x3);
+    lx0 = ptx::f2_add(lx0, ptx::f2(p0, p1));
+    lx1 = ptx::f2_add(lx1, ptx::f2(p2, p3));
+    pk[c / 2] = ptx::pack2<BF16>(p0, p1);
+    pk[c / 2 + 1] = ptx::pack2<BF16>(p2, p3);
+    // the denominator sums the same 16-bit values the P.V product sees
+    lp0 = ptx::add_lo16<BF16>(lp0, pk[c / 2]);
+    lp1 = ptx::add_hi16<BF16>(lp1, pk[c / 2]);
+    lp2 = ptx::add_lo16<BF16>(lp2, pk[c / 2 + 1]);
+    lp3 = ptx::add_hi16<BF16>(lp3, pk[c / 2 + 1]);
+  }
+  ptx::tmem_st_x32(tP, pk);
+  float a0, a1, b0, b1;
+  ptx::f2_split(lx0, a0, a1);
+  ptx::f2_split(lx1, b0, b1);
+  st.l_x = st.l_x * alpha + ((a0 + a1) + (b0 + b1));
+  st.l_p = st.l_p * alpha + ((lp0 + lp1) + (lp2 + lp3));
+
+  if (!first && __any_sync(0xffffffffu, rescale)) {
+    if (!wait_bar_warp(pvd_bar, pvd_parity, ctl)) return false;
+    ptx::tc_fence_after();
+    const uint64_t al2 = ptx::f2(alpha, alpha);
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      uint32_t o[32];
+      ptx::tmem_ld_x32(tO + c0, o);
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        float a, b;
+        ptx::f2_split(
+            ptx::f2_mul(ptx::f2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), al2), a, b);
+        o[i] = __float_as_uint(a);
+        o[i + 1] = __float_as_uint(b);
+      }
+      ptx::tmem_st_x32(tO + c0, o);
+    }
+  }
+  ptx::tmem_wait_st();
+  return true;
+}
+
 template <bool BF16>
 __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, uint32_t bars,
-                             const Ctl& ctl) {
+                             uint8_t* base, const Ctl& ctl) {
   using L = Layout;
-  const int warp = threadIdx.x >> 5;  // 0..3
+  const int warp = threadIdx.x >> 5;  // 0..7
   const int lane = threadIdx.x & 31;
-  const int row = warp * 32 + lane;
-  const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t tO = tmem + lane_bits + L::kColO;
+  const int quarter = warp & 3;       // TMEM lane quarter (= SM sub-partition)
+  const int half = warp >> 2;         // columns [64 half, 64 half + 64) of S and O
+  const int row = quarter * 32 + lane;
+  const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
+  const uint32_t tO = tmem + lane_bits + L::kColO + half * 64;
   const uint32_t bar_p_lead = ptx::mapa(bars + 8 * L::PF, 0);  // + 8 * (G % 3)
   const uint32_t bar_o = bars + 8 * L::OF;
+  const uint32_t xbar = 1 + quarter;  // named barrier of the two warps of these rows
+  float* const xmax = reinterpret_cast<float*>(base + L::kXMaxOff);  // [parity][half][row]
+  float* const xsum = reinterpret_cast<float*>(base + L::kXSumOff);  // [half][row][2]
   uint32_t o_cnt = 0, g_base = 0;
   uint16_t* const O = static_cast<uint16_t*>(p.o);
 
@@ -142,25 +255,33 @@ __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, u
         if (!wait_bar_warp(bars + 8 * (L::SF + b), (G / kNBuf) & 1u, ctl)) return;
         ptx::tc_fence_after();
         int limit = p.causal ? min(127, qrow - j * kBN) : 127;
-        limit = min(limit, w.Lk - j * kBN - 1);
+        limit = min(limit, w.Lk - j * kBN - 1) - 64 * half;
         // O += P(G-1) V(G-1) may still be running: a rescale of O waits for it.
         const uint32_t gp = G - 1;
-        if (!softmax_step_pv<D, BF16>(tmem + lane_bits + L::kColS + b * 128, tO, limit,
-                                      p.scale_log2, p.scale_pos != 0, j == 0, rs,
-                                      bars + 8 * (L::PVD + gp % kNBuf), (gp / kNBuf) & 1u,
-                                      ctl))
+        float* const xm = xmax + (G & 1u) * 256;
+        const uint32_t tSb = tmem + lane_bits + L::kColS + b * 128;
+        if (!softmax_half_step<BF16>(tSb + 64 * half, tSb + 32 * half, tO, limit, p.scale_log2,
+                                     p.scale_pos != 0, j == 0, rs, xm + half * 128 + row,
+                                     xm + (1 - half) * 128 + row, xbar,
+                                     bars + 8 * (L::PVD + gp % kNBuf), (gp / kNBuf) & 1u, ctl))
           return;
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive_cluster_relaxed(bar_p_lead + 8u * b);
       }
       g_base += n;
+      // both halves' sums are relative to the same running max: add them
+      xsum[(half * 128 + row) * 2 + 0] = rs.l_p;
+      xsum[(half * 128 + row) * 2 + 1] = rs.l_x;
+      ptx::named_bar_sync(xbar, 64);
+      rs.l_p += xsum[((1 - half) * 128 + row) * 2 + 0];
+      rs.l_x += xsum[((1 - half) * 128 + row) * 2 + 1];
       if (!wait_bar_warp(bar_o, o_cnt & 1u, ctl)) return;
       ++o_cnt;
       ptx::tc_fence_after();
       const float inv_l = rs.l_p > 0.0f ? 1.0f / rs.l_p : 0.0f;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t o[32];
         ptx::tmem_ld_x32(tO + c0, o);
         uint32_t pk[16];
@@ -169,18 +290,18 @@ __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, u
           pk[i] = ptx::pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
                                    __uint_as_float(o[2 * i + 1]) * inv_l);
         if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(O + orow * D + c0);
+          uint4* dst = reinterpret_cast<uint4*>(O + orow * D + half * 64 + c0);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
       }
     } else if (row_ok) {  // no visible key at all: O = 0, LSE = -inf
-      uint4* dst = reinterpret_cast<uint4*>(O + orow * D);
+      uint4* dst = reinterpret_cast<uint4*>(O + orow * D + half * 64);
 #pragma unroll
-      for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      for (int i = 0; i < 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
     }
-    if (row_ok) {
+    if (row_ok && half == 0) {
       p.lse[lidx] = rs.l_x > 0.0f ? (rs.m + ptx::lg2(rs.l_x)) * 0.69314718055994531f : -INFINITY;
     }
   }
@@ -378,8 +499,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Ctl ctl{abort_flag, p.err, p.timeout_ns};
 
-  if (warp < kPMma) {
-    softmax_role<BF16>(p, rank, tmem, bars, ctl);
+  if (warp < kSoftmaxWarps) {
+    softmax_role<BF16>(p, rank, tmem, bars, base, ctl);
   } else if (warp == kPMma) {
     if (lane == 0 && rank == 0) {
       s_loop<BF16>(p, smem, tmem, bars, ctl);

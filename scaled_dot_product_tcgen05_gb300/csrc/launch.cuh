@@ -30,14 +30,14 @@ inline long long units_bound(bool varlen, int B, int H, long long rows_q, int Sq
                 : static_cast<long long>(B) * H * ((Sq + rows_per_unit - 1) / rows_per_unit);
 }
 
-// The single-CTA kernel runs by default.  ATTN_PAIR=1 selects the CTA-pair
-// kernel (2-SM MMAs) for head dim 128.  The grid is persistent: at most one
-// CTA per SM.
+// Head dim 128 runs on CTA pairs with 2-SM MMAs; head dim 64 on single CTAs.
+// ATTN_PAIR=0 sends head dim 128 to the single-CTA kernel as well (kept for
+// cross-checks).  The grid is persistent: at most one CTA per SM.
 inline cudaError_t launch_forward(const FwdParams& p, int D, bool bf16, bool varlen, int B, int H,
                                   long long rows_q, int Sq, int sms, cudaStream_t s,
                                   LaunchInfo* info) {
   const char* sel = std::getenv("ATTN_PAIR");
-  const bool use_pair = D == 128 && sms >= 2 && sel != nullptr && sel[0] == '1';
+  const bool use_pair = D == 128 && sms >= 2 && !(sel != nullptr && sel[0] == '0');
   if (use_pair) {
     const long long units = units_bound(varlen, B, H, rows_q, Sq, pair::kUR);
     const long long pairs = units < sms / 2 ? units : sms / 2;

@@ -189,7 +189,32 @@ def test_grid_is_persistent():
     q, k, v = _dense_case(6, 1, 32, 4096, 4096, 128, torch.bfloat16)
     run_gpu(q, k, v, True, 0.088)
     grid, smem = pkg.last_launch()
+    assert grid == 2 * (pkg.num_sms() // 2) and smem <= 232448
+    q, k, v = _dense_case(7, 1, 32, 4096, 4096, 64, torch.bfloat16)
+    run_gpu(q, k, v, True, 0.125)
+    grid, smem = pkg.last_launch()
     assert grid == pkg.num_sms() and smem <= 232448
+
+
+@pytest.mark.parametrize("case", [
+    (2, 3, 700, 700, torch.bfloat16, True),
+    (1, 2, 300, 520, torch.float16, False),
+], ids=["dense_bf16_causal", "dense_fp16_q300_k520"])
+def test_single_cta_kernel_head_dim_128(case, monkeypatch):
+    """Head dim 128 runs on CTA pairs; ATTN_PAIR=0 keeps the single-CTA kernel covered."""
+    monkeypatch.setenv("ATTN_PAIR", "0")
+    B, H, Sq, Sk, dt, causal = case
+    q, k, v = _dense_case(Sq + 3 * Sk, B, H, Sq, Sk, 128, dt)
+    o, lse = run_gpu(q, k, v, causal, 1 / math.sqrt(128))
+    grid, _ = pkg.last_launch()
+    assert grid <= pkg.num_sms()
+    o_ref, l_ref = attention_dense(q, k, v, 1 / math.sqrt(128), causal)
+    compare(o, lse, o_ref, l_ref, what=f"1sm {case}")
+    lens = [300, 1, 129, 0, 900]
+    qv, kv, vv, cq, ck = _varlen(13, lens, lens, 2, 128, torch.bfloat16)
+    o, lse = run_gpu(qv, kv, vv, True, 0.1, cq, ck)
+    o_ref, l_ref = attention_varlen(qv, kv, vv, cq, ck, 0.1, True)
+    compare(o, lse, o_ref, l_ref, what="1sm varlen")
 
 
 PAIR_CASES = [
@@ -202,9 +227,8 @@ PAIR_CASES = [
 
 @pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: "B{}H{}q{}k{}{}{}".format(
     c[0], c[1], c[2], c[3], "bf" if c[4] == torch.bfloat16 else "fp", "c" if c[5] else ""))
-def test_cta_pair_kernel(case, monkeypatch):
-    """Head dim 128 on CTA pairs (2-SM MMAs), selected with ATTN_PAIR=1."""
-    monkeypatch.setenv("ATTN_PAIR", "1")
+def test_cta_pair_kernel(case):
+    """Head dim 128 on CTA pairs (2-SM MMAs)."""
     B, H, Sq, Sk, dt, causal = case
     q, k, v = _dense_case(Sq + 5 * Sk, B, H, Sq, Sk, 128, dt)
     o, lse = run_gpu(q, k, v, causal, 1 / math.sqrt(128))
@@ -214,8 +238,7 @@ def test_cta_pair_kernel(case, monkeypatch):
     compare(o, lse, o_ref, l_ref, what=f"pair {case}")
 
 
-def test_cta_pair_kernel_varlen(monkeypatch):
-    monkeypatch.setenv("ATTN_PAIR", "1")
+def test_cta_pair_kernel_varlen():
     for causal in (False, True):
         lens_q = [1, 0, 300, 129, 5, 256, 1000]
         lens_k = [1, 7, 300, 129, 0, 100, 1000]
