@@ -31,7 +31,7 @@ import torch  # noqa: E402
 from scaled_dot_product_tcgen05_gb300 import workloads as W  # noqa: E402
 
 DEFAULT_WORKLOAD = "long64k_causal"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attn_fwd_kernel_long64k_causal.md")
+PROFILE_DIR = os.path.join(ROOT, "profiles")
 FALLBACK_PEAK_TFLOPS = 1900.0
 
 
@@ -148,11 +148,18 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def kernel_name(D: int) -> str:
+    """The kernel attn_fwd launches (head dim 128 runs on CTA pairs unless ATTN_PAIR=0)."""
+    return "attn_fwd_kernel_2sm" if D == 128 and os.environ.get("ATTN_PAIR") != "0" \
+        else "attn_fwd_kernel"
+
+
+def profiled_traffic(workload: str, kernel: str):
     """Per-launch DRAM bytes from the committed ncu summary, if it matches the sources."""
-    if not os.path.exists(PROFILE_SUMMARY) or workload != DEFAULT_WORKLOAD:
+    path = os.path.join(PROFILE_DIR, f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
         return None
-    text = open(PROFILE_SUMMARY).read()
+    text = open(path).read()
     m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     m_h = re.search(r"source_digest:\s*([0-9a-f]+)", text)
     if not (m_t and m_h) or m_h.group(1) != source_digest():
@@ -376,7 +383,8 @@ def main(argv=None):
         return 0
     peak, peak_src = peaks()
     achieved = flops / (kernel_ms * 1e-3) / 1e12
-    traffic = profiled_traffic(wl.name)
+    kern = kernel_name(wl.D)
+    traffic = profiled_traffic(wl.name, kern)
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_sample(wl, args.cpu_budget_s)
@@ -392,7 +400,7 @@ def main(argv=None):
         "pct_of_peak": achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
-                     "kernel": "attn_fwd_kernel", "kernel_ms": kernel_ms},
+                     "kernel": kern, "kernel_ms": kernel_ms},
         "e2e": {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
