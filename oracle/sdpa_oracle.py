@@ -17,6 +17,12 @@ written out step by step as an unfused pipeline:
     cu_seqlens_q[b]:cu_seqlens_q[b+1] and key rows cu_seqlens_k[b]:cu_seqlens_k[b+1]
     and never sees another sequence (page "长文本处理性能断层真相", §1, the
     varlen call with int32 cu_seqlens);
+  * sliding window + global rows (page "长文本处理性能断层真相", §2.5, the hybrid
+    of a local-window attention for every query and full attention for the
+    first global_tokens queries, spliced row-wise): query i >= global_q sees
+    key j only when i - window_left <= j <= i + window_right (-1: that side
+    unbounded); query i < global_q sees every key.  The causal rule applies on
+    top of both;
   * a full-row softmax (row max, exp, sum, divide), then P V;
   * the per-row logsumexp LSE_i = max_j s_ij + ln sum_j exp(s_ij - max_j s_ij),
     natural log, over the scaled and masked scores.
@@ -29,7 +35,12 @@ Readings where the pages are silent:
   * a row with no visible key (only possible for an empty key sequence) gives
     O = 0 and LSE = -inf;
   * causal alignment is top-left (the literal i >= j test), so it also holds
-    when a sequence has Sq != Sk.
+    when a sequence has Sq != Sk;
+  * the page sizes its window by one number (window_size); here the two sides
+    of the band are given separately and include their end points, so a causal
+    window of W keys (the query and the W-1 keys before it) is window_left =
+    W - 1, window_right = 0; the page's "full attention" for the global rows
+    keeps the causal rule when the call is causal.
 
 Parity status: every function here is pinned by tests/test_oracle.py (brute
 force, closed forms, invariants, a library routine); none is "parity unpinned".
@@ -49,14 +60,33 @@ def _as_f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
+def visible_mask(row_idx: np.ndarray, Sk: int, causal: bool, window_left: int = -1,
+                 window_right: int = -1, global_q: int = 0) -> np.ndarray:
+    """visible[r, j]: may query row_idx[r] see key j (indices within the sequence)."""
+    i = np.asarray(row_idx, dtype=np.int64)[:, None]
+    j = np.arange(Sk, dtype=np.int64)[None, :]
+    visible = np.ones((i.shape[0], Sk), dtype=bool)
+    banded = i >= global_q          # global rows ignore the window
+    if window_left >= 0:
+        visible &= ~banded | (j >= i - window_left)
+    if window_right >= 0:
+        visible &= ~banded | (j <= i + window_right)
+    if causal:
+        visible &= j <= i
+    return visible
+
+
 def attention_one_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
                        causal: bool, rows: Optional[Sequence[int]] = None,
-                       return_p: bool = False):
+                       return_p: bool = False, window_left: int = -1, window_right: int = -1,
+                       global_q: int = 0):
     """Attention for one (sequence, head).
 
     q [Sq, D], k [Sk, D], v [Sk, Dv] in fp64.  ``rows`` restricts the output to
-    those query indices (indices within the sequence).  Returns (O [R, Dv],
-    LSE [R]) and, when ``return_p``, the probability matrix P [R, Sk].
+    those query indices (indices within the sequence).  ``window_left``,
+    ``window_right`` and ``global_q`` add the sliding-window mask (defaults:
+    none).  Returns (O [R, Dv], LSE [R]) and, when ``return_p``, the probability
+    matrix P [R, Sk].
     """
     Sq = q.shape[0]
     Sk = k.shape[0]
@@ -65,9 +95,7 @@ def attention_one_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float
     # step 1: all scores, materialised
     s = scale * (qs @ k.T)                                   # [R, Sk]
     # step 2: mask -> visible[i, j]
-    visible = np.ones(s.shape, dtype=bool)
-    if causal:
-        visible &= np.arange(Sk)[None, :] <= row_idx[:, None]
+    visible = visible_mask(row_idx, Sk, causal, window_left, window_right, global_q)
     s_masked = np.where(visible, s, -np.inf)
     # step 3: full-row softmax
     has_key = visible.any(axis=1)
@@ -86,7 +114,8 @@ def attention_one_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float
 
 def attention_dense(q, k, v, scale: float, causal: bool,
                     heads: Optional[Sequence[int]] = None,
-                    rows: Optional[Sequence[int]] = None):
+                    rows: Optional[Sequence[int]] = None, window_left: int = -1,
+                    window_right: int = -1, global_q: int = 0):
     """Dense batch: q [B,Sq,H,D], k/v [B,Sk,H,D] -> O [B,Sq,H,D], LSE [B,H,Sq].
 
     With ``heads``/``rows`` only those heads/query rows are computed; the others
@@ -101,14 +130,16 @@ def attention_dense(q, k, v, scale: float, causal: bool,
     for b in range(B):
         for h in (range(H) if heads is None else heads):
             ob, lb = attention_one_head(q[b, :, h, :], k[b, :, h, :], v[b, :, h, :],
-                                        scale, causal, rows=row_sel)
+                                        scale, causal, rows=row_sel, window_left=window_left,
+                                        window_right=window_right, global_q=global_q)
             o[b, row_sel, h, :] = ob
             lse[b, h, row_sel] = lb
     return o, lse
 
 
 def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool,
-                     heads: Optional[Sequence[int]] = None):
+                     heads: Optional[Sequence[int]] = None, window_left: int = -1,
+                     window_right: int = -1, global_q: int = 0):
     """Packed varlen batch: q [Tq,H,D], k/v [Tk,H,D] -> O [Tq,H,D], LSE [H,Tq].
 
     Rows of q that belong to no sequence are returned as NaN.
@@ -126,7 +157,8 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: 
             continue
         for h in (range(H) if heads is None else heads):
             ob, lb = attention_one_head(q[q0:q1, h, :], k[k0:k1, h, :], v[k0:k1, h, :],
-                                        scale, causal)
+                                        scale, causal, window_left=window_left,
+                                        window_right=window_right, global_q=global_q)
             o[q0:q1, h, :] = ob
             lse[h, q0:q1] = lb
     return o, lse
