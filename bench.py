@@ -3,7 +3,9 @@
 One step = one fused forward (O and LSE) over the long-context causal workload
 B=1, H=32, Sq=Sk=65536, D=128, bf16 (inputs 1.5 GiB, larger than the 129 MB
 L2, so no flush is needed between steps).  Throughput is TFLOP/s with the
-FLOP count 4*B*H*Sq*Sk*D, halved for causal.
+FLOP count 4*B*H*Sq*Sk*D, halved for causal; for a sliding-window workload
+(--workload window128k_causal) 4*D per visible (query, key) pair, counted
+exactly.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   (the fp64 CPU oracle on a bounded sample)
@@ -172,6 +174,9 @@ def workload_info(wl):
         lens = W.varlen_lengths(wl).tolist()
         flops = W.varlen_flops(lens, wl.H, wl.D, wl.causal)
         tokens = sum(lens)
+    elif wl.windowed:  # exact count of visible (query, key) pairs
+        flops = W.window_flops(wl.B, wl.H, wl.Sq, wl.Sk, wl.D, wl.causal, wl.window, wl.global_q)
+        tokens = wl.B * wl.Sq
     else:
         flops = W.attention_flops(wl.B, wl.H, wl.Sq, wl.Sk, wl.D, wl.causal)
         tokens = wl.B * wl.Sq
@@ -182,7 +187,20 @@ def workload_info(wl):
            "Sk": wl.Sk if not wl.varlen else tokens, "D": wl.D, "causal": wl.causal,
            "dtype": wl.dtype, "varlen": wl.varlen, "flops_per_step": flops,
            "algorithmic_bytes_per_step": nbytes}
+    if wl.windowed:
+        cfg.update(window=list(wl.window), global_q=wl.global_q)
     return flops, nbytes, cfg
+
+
+def _mask_kw(wl):
+    """Oracle keyword arguments of the workload's mask."""
+    return dict(window_left=wl.window[0], window_right=wl.window[1], global_q=wl.global_q)
+
+
+def _row_keys(wl, rows):
+    """Visible keys of the given query rows (for the sampled FLOP counts)."""
+    counts = W.visible_key_counts(wl.Sq, wl.Sk, wl.causal, wl.window, wl.global_q)
+    return [int(counts[i]) for i in rows]
 
 
 # ------------------------------------------------------------------ reference (oracle)
@@ -202,19 +220,16 @@ def run_reference(args, wl, flops_full, cfg):
     qf = {h: q[:, h].double().numpy() for h in heads}
     kf = {h: k[:, h].double().numpy() for h in heads}
     vf = {h: v[:, h].double().numpy() for h in heads}
-    sample_flops = 0.0
-    for h in heads:
-        for i in rows:
-            keys = (i + 1) if wl.causal else wl.Sk
-            sample_flops += 4.0 * keys * wl.D
+    sample_flops = 4.0 * wl.D * len(heads) * sum(_row_keys(wl, rows))
     times = []
     for _ in range(args.warmup):
         attention_one_head(qf[heads[0]], kf[heads[0]], vf[heads[0]], wl.scale, wl.causal,
-                           rows=rows[: max(1, len(rows) // 8)])
+                           rows=rows[: max(1, len(rows) // 8)], **_mask_kw(wl))
     for _ in range(args.steps):
         t0 = time.perf_counter()
         for h in heads:
-            attention_one_head(qf[h], kf[h], vf[h], wl.scale, wl.causal, rows=rows)
+            attention_one_head(qf[h], kf[h], vf[h], wl.scale, wl.causal, rows=rows,
+                               **_mask_kw(wl))
         times.append(time.perf_counter() - t0)
     t = sum(times) / len(times)
     value = sample_flops / t / 1e12
@@ -260,9 +275,9 @@ def cpu_baseline_sample(wl, budget_s: float):
     while spent < budget_s and n < S:
         rows = sorted(rows_all[n:n + chunk].tolist())
         t0 = time.perf_counter()
-        attention_one_head(q, k, v, wl.scale, wl.causal, rows=rows)
+        attention_one_head(q, k, v, wl.scale, wl.causal, rows=rows, **_mask_kw(wl))
         spent += time.perf_counter() - t0
-        done_flops += sum(4.0 * ((i + 1) if wl.causal else wl.Sk) * wl.D for i in rows)
+        done_flops += 4.0 * wl.D * sum(_row_keys(wl, rows))
         n += chunk
     return {"value": done_flops / spent / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
             "kind": "oracle",
@@ -319,7 +334,8 @@ def main(argv=None):
 
     def step():
         pkg.attn_fwd(q, k, v, causal=wl.causal, scale=wl.scale, cu_seqlens_q=cu,
-                     cu_seqlens_k=cu, out=o, lse=lse, stream=stream)
+                     cu_seqlens_k=cu, out=o, lse=lse, window=wl.window, global_q=wl.global_q,
+                     stream=stream)
 
     # ---- kernel-only timed region (inputs resident in HBM)
     for _ in range(args.warmup):

@@ -78,6 +78,35 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int dtype, void* stream);
 
 /*
+ * attn_fwd_window -- attn_fwd with a sliding-window mask and global query rows.
+ *
+ * The mask follows the "sliding window + global tokens" scheme of page
+ * "长文本处理性能断层真相" (lnrk.cn), §2.5, for 128K-token contexts: every
+ * query attends to a band of nearby keys, and the first global_q queries of
+ * each sequence attend to all keys.  With indices i (query) and j (key) inside
+ * one sequence, key j is visible to query i when
+ *   i >= global_q:  i - window_left <= j <= i + window_right   (and j <= i if causal)
+ *   i <  global_q:  always                                      (j <= i if causal)
+ * window_left / window_right = -1 leave that side unbounded, so
+ * attn_fwd_window(..., -1, -1, 0, ...) computes exactly attn_fwd.  A causal
+ * sliding window of W keys (the query itself and the W-1 before it) is
+ * window_left = W - 1, window_right = 0 (or -1), causal = 1.
+ *
+ * Arguments, layouts, ownership, stream semantics and errors as attn_fwd, and:
+ *   window_left, window_right  >= -1, else ATTN_ERR_INVALID_ARG; with causal
+ *                              set, window_right > 0 is ATTN_ERR_INVALID_ARG.
+ *   global_q                   >= 0, else ATTN_ERR_INVALID_ARG.
+ * A row that sees no key gets O = 0 and LSE = -inf.  K/V tiles that no row of
+ * a query tile can see are skipped, so the work grows with the band width, not
+ * with Sk.
+ */
+int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int H, int Sq, int Sk, int D, float scale, int causal,
+                    int window_left, int window_right, int global_q,
+                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                    int dtype, void* stream);
+
+/*
  * attn_check -- synchronise `stream`, then report and clear the device error
  * word of the current device: ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT,
  * ATTN_ERR_BAD_SEQLENS, or ATTN_ERR_CUDA if the stream itself failed.

@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     attn_check,
     attn_fwd,
     attn_fwd_raw,
+    attn_fwd_window_raw,
     last_launch,
     load_library,
     num_sms,

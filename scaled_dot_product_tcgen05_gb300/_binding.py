@@ -28,7 +28,7 @@ ATTN_ERR_BAD_SEQLENS = -6
 DTYPE_CODES = {torch.float16: 0, torch.bfloat16: 1}
 
 EXPORTED = ("attn_fwd", "attn_check", "attn_status_string", "attn_num_sms",
-            "attn_last_launch", "attn_release", "attn_fwd_noalloc")
+            "attn_last_launch", "attn_release", "attn_fwd_noalloc", "attn_fwd_window")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -56,6 +56,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, i, vp]
         lib.attn_fwd.restype = i
+        lib.attn_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i, i, vp, vp,
+                                        i, vp]
+        lib.attn_fwd_window.restype = i
         lib.attn_check.argtypes = [vp]
         lib.attn_check.restype = i
         lib.attn_status_string.argtypes = [i]
@@ -94,17 +97,34 @@ def attn_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B
                                    dtype_code, stream or None)
 
 
+def attn_fwd_window_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int,
+                        H: int, Sq: int, Sk: int, D: int, scale: float, causal: bool,
+                        window_left: int, window_right: int, global_q: int, cu_q_ptr: int,
+                        cu_k_ptr: int, dtype_code: int, stream: int) -> int:
+    """Direct call of the windowed C entry point; returns the status."""
+    return load_library().attn_fwd_window(
+        q_ptr or None, k_ptr or None, v_ptr or None, o_ptr or None, lse_ptr or None, B, H, Sq, Sk,
+        D, ctypes.c_float(scale), 1 if causal else 0, int(window_left), int(window_right),
+        int(global_q), cu_q_ptr or None, cu_k_ptr or None, dtype_code, stream or None)
+
+
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = False,
              scale: Optional[float] = None, cu_seqlens_q: Optional[torch.Tensor] = None,
              cu_seqlens_k: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
-             lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+             lse: Optional[torch.Tensor] = None, window: Tuple[int, int] = (-1, -1),
+             global_q: int = 0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Fused attention forward on the GPU.  Returns (O, LSE).
 
     dense : q [B,Sq,H,D], k/v [B,Sk,H,D] -> O like q, LSE fp32 [B,H,Sq]
     varlen: q [Tq,H,D], k/v [Tk,H,D], int32 cu_seqlens [B+1] -> O like q, LSE [H,Tq]
     ``scale`` defaults to 1/sqrt(D).  ``causal`` keeps key j for query i iff j <= i
-    (indices inside each sequence).  The launch is asynchronous on ``stream``
-    (default: torch's current stream); device-side errors are reported by
+    (indices inside each sequence).  ``window = (left, right)`` keeps only keys
+    i - left <= j <= i + right (-1: that side unbounded; causal needs right <= 0)
+    for the query rows i >= ``global_q``; the first ``global_q`` rows of each
+    sequence attend to every key (up to the diagonal when causal).  The default
+    runs the ``attn_fwd`` entry point, any window or global rows
+    ``attn_fwd_window``.  The launch is asynchronous on ``stream`` (default:
+    torch's current stream); device-side errors are reported by
     :func:`attn_check`.
     """
     varlen = cu_seqlens_q is not None or cu_seqlens_k is not None
@@ -151,14 +171,22 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool 
         lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
     elif tuple(lse.shape) != lse_shape or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError(f"lse must be a contiguous fp32 tensor of shape {lse_shape}")
+    wl, wr = (int(x) for x in window)
+    windowed = (wl, wr) != (-1, -1) or int(global_q) != 0
     with torch.cuda.device(q.device):
-        st = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                          lse.data_ptr(), B, H, Sq, Sk, D, float(scale), causal,
-                          cu_seqlens_q.data_ptr() if varlen else 0,
-                          cu_seqlens_k.data_ptr() if varlen else 0, DTYPE_CODES[q.dtype],
-                          _stream_handle(stream))
+        cq = cu_seqlens_q.data_ptr() if varlen else 0
+        ck = cu_seqlens_k.data_ptr() if varlen else 0
+        if windowed:
+            st = attn_fwd_window_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                     lse.data_ptr(), B, H, Sq, Sk, D, float(scale), causal, wl,
+                                     wr, int(global_q), cq, ck, DTYPE_CODES[q.dtype],
+                                     _stream_handle(stream))
+        else:
+            st = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr(), B, H, Sq, Sk, D, float(scale), causal, cq, ck,
+                              DTYPE_CODES[q.dtype], _stream_handle(stream))
     if st != ATTN_OK:
-        raise AttnError(st, "attn_fwd")
+        raise AttnError(st, "attn_fwd_window" if windowed else "attn_fwd")
     return out, lse
 
 

@@ -111,12 +111,17 @@ int encode_rows_heads_dim(CUtensorMap* m, const void* ptr, long long rows, int H
 
 using namespace attn;
 
-extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                        int H, int Sq, int Sk, int D, float scale, int causal,
-                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int dtype,
-                        void* stream) {
+namespace attn {
+namespace {
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int Sq, int Sk, int D, float scale, int causal, int window_left, int window_right,
+             int global_q, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int dtype,
+             void* stream) {
   // ---- argument checks (no CUDA call before these pass)
   if (B < 0 || H < 1 || Sq < 0 || Sk < 1) return ATTN_ERR_INVALID_ARG;
+  FwdParams p;
+  if (!set_mask(p, causal, window_left, window_right, global_q)) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (dtype != ATTN_DTYPE_FP16 && dtype != ATTN_DTYPE_BF16) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -152,7 +157,6 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     return ATTN_ERR_INVALID_ARG;
 
   // ---- parameters
-  FwdParams p;
   const bool bf16 = dtype == ATTN_DTYPE_BF16;
   if (encode_rows_heads_dim(&p.tm_q, q, rows_q, H, D, bf16) != ATTN_OK ||
       encode_rows_heads_dim(&p.tm_k, k, rows_k, H, D, bf16) != ATTN_OK ||
@@ -169,7 +173,6 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   p.Sq = Sq;
   p.Sk = Sk;
   p.varlen = varlen ? 1 : 0;
-  p.causal = causal ? 1 : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.scale_pos = scale > 0.0f ? 1 : 0;
   p.timeout_ns = timeout_ns_from_env();
@@ -184,6 +187,26 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   t_last_grid = info.grid;
   t_last_smem = info.smem;
   return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int Sq, int Sk, int D, float scale, int causal,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int dtype,
+                        void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, -1, -1, 0, cu_seqlens_q,
+                  cu_seqlens_k, dtype, stream);
+}
+
+extern "C" int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int H, int Sq, int Sk, int D, float scale, int causal,
+                               int window_left, int window_right, int global_q,
+                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                               int dtype, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, window_left, window_right,
+                  global_q, cu_seqlens_q, cu_seqlens_k, dtype, stream);
 }
 
 extern "C" int attn_check(void* stream) {

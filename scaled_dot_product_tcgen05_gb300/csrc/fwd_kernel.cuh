@@ -44,6 +44,7 @@ constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;     // rescale O only if max grows by > 2^8
+constexpr int kUnbounded = 1 << 30;      // window side without a bound
 
 enum : int { kErrTimeout = 1, kErrBadSeqlens = 2 };
 
@@ -59,6 +60,11 @@ struct FwdParams {
   int* err;                  // device error word (bit flags above)
   int B, H, Sq, Sk;          // dense: per-batch lengths; varlen: total packed rows
   int varlen, causal;
+  // Visibility of key j to query i (indices within the sequence): rows
+  // i >= global_q see keys i - win_left <= j <= i + win_right; rows
+  // i < global_q see every key (j <= i when causal).  An unbounded side is
+  // kUnbounded; causal sets win_right = 0.
+  int win_left, win_right, global_q;
   float scale_log2;          // scale * log2(e)
   int scale_pos;             // scale > 0: fold the scale into the exp2 argument
   long long timeout_ns;      // limit for any single pipeline wait
@@ -123,6 +129,7 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, con
 struct Unit {
   int b, h, qt;               // sequence, head, unit index within the sequence
   int q_start, Lq, k_start, Lk;
+  int j0;                     // first K/V tile visited (step j reads tile j0 + j)
   int n[kTiles];              // K/V tiles visited by each query tile
   bool valid[kTiles];         // tile holds at least one real query row
 };
@@ -202,23 +209,56 @@ __device__ __forceinline__ bool decode_rows(const FwdParams& p, int u, Cursor& c
   return true;
 }
 
-// K/V tiles a 128-row query tile starting at row q0 must visit (0: none).
-__device__ __forceinline__ int tiles_for(const FwdParams& p, const Unit& w, int q0) {
-  if (q0 >= w.Lq) return 0;
+// K/V tiles [lo, hi) holding every key that some row of the 128-row query
+// tile starting at row q0 can see (hi <= lo: none).  Tiles outside the range
+// are never loaded or multiplied; keys inside it that a row cannot see are
+// masked in the softmax.
+__device__ __forceinline__ void tile_keys(const FwdParams& p, const Unit& w, int q0, int& lo,
+                                          int& hi) {
+  lo = hi = 0;
+  if (q0 >= w.Lq) return;
+  const int q1 = min(q0 + kBM, w.Lq) - 1;
   const int nk = (w.Lk + kBN - 1) / kBN;
-  // causal: rows q0..q0+127 see keys <= their index, so tiles up to the diagonal
-  return p.causal ? min(nk, q0 / kBN + 1) : nk;
+  if (q0 < p.global_q) {  // rows that see every key (up to the diagonal when causal)
+    hi = p.causal ? min(nk, q1 / kBN + 1) : nk;
+    return;
+  }
+  // rows q0..q1 see keys q0 - win_left .. q1 + win_right
+  lo = max(0, q0 - p.win_left) / kBN;
+  hi = static_cast<int>(min(static_cast<long long>(nk),
+                            (static_cast<long long>(q1) + p.win_right) / kBN + 1));
+}
+
+// Keys lo..hi (inclusive, indices within the sequence) that query row qrow
+// may see; once per unit.  Step j masks columns c of tile j0 + j outside
+// lo - kb .. hi - kb, kb = (j0 + j) * 128.
+__device__ __forceinline__ void row_keys(const FwdParams& p, const Unit& w, int qrow, int& lo,
+                                         int& hi) {
+  hi = w.Lk - 1;
+  lo = 0;
+  if (qrow >= p.global_q) {  // qrow + win_right and qrow - win_left without overflow
+    hi = qrow > hi - p.win_right ? hi : qrow + p.win_right;
+    lo = qrow > p.win_left ? qrow - p.win_left : 0;
+  } else if (p.causal) {
+    hi = min(hi, qrow);
+  }
 }
 
 __device__ __forceinline__ bool decode_unit(const FwdParams& p, int u, Cursor& c, Unit& w,
                                             bool report) {
   if (!decode_rows<kUnitRows>(p, u, c, w, report)) return false;
+  int lo[kTiles], hi[kTiles];
 #pragma unroll
   for (int t = 0; t < kTiles; ++t) {
     const int q0 = w.qt * kUnitRows + t * kBM;
     w.valid[t] = q0 < w.Lq;
-    w.n[t] = tiles_for(p, w, q0);
+    tile_keys(p, w, q0, lo[t], hi[t]);
   }
+  // both query tiles walk the K/V tiles from the first one either needs
+  // (tile 0's, the smaller); each stops at its own last tile
+  w.j0 = lo[0];
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t) w.n[t] = w.valid[t] ? max(0, hi[t] - w.j0) : 0;
   return true;
 }
 
@@ -243,7 +283,8 @@ struct RowState {
 };
 
 // One K/V tile of the online softmax for the calling thread's query row.
-// S is read from TMEM (128 fp32 columns), masked (keys c > limit are invisible),
+// S is read from TMEM (128 fp32 columns), masked (keys c < lo or c > limit are
+// invisible),
 // turned into P = 2^(scale*log2e*s - m) rounded to 16 bits and written back over
 // the first 64 columns of S.  O is rescaled in TMEM when the running max moved
 // by more than 2^kRescaleLog2; otherwise the stale max is kept for P and l,
@@ -251,7 +292,8 @@ struct RowState {
 // pvd_bar != 0: before rescaling O, wait (parity pvd_parity) for the MMA that
 // accumulates the previous tile into O; returns false if that wait gave up.
 template <int D, bool BF16>
-__device__ __forceinline__ bool softmax_step_pv(uint32_t tS, uint32_t tO, int limit, float cl,
+__device__ __forceinline__ bool softmax_step_pv(uint32_t tS, uint32_t tO, int lo, int limit,
+                                                float cl,
                                                 bool scale_pos, bool first, RowState& st,
                                                 uint32_t pvd_bar, uint32_t pvd_parity,
                                                 const Ctl& ctl) {
@@ -270,10 +312,10 @@ __device__ __forceinline__ bool softmax_step_pv(uint32_t tS, uint32_t tO, int li
     }
     cle = 1.0f;
   }
-  if (limit < 127) {
+  if (limit < 127 || lo > 0) {
 #pragma unroll
     for (int c = 0; c < 128; ++c)
-      if (c > limit) r[c] = __float_as_uint(-INFINITY);
+      if (c > limit || c < lo) r[c] = __float_as_uint(-INFINITY);
   }
   float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
@@ -378,15 +420,16 @@ __device__ void softmax_role(const FwdParams& p, int t, uint32_t tmem, uint32_t 
                                : (static_cast<long long>(w.b) * p.H + w.h) * p.Sq + qrow;
     RowState rs{-INFINITY, 0.0f, 0.0f};
     if (n > 0) {
-      const int diag = q0 / kBN;
-      for (int j = 0; j < n; ++j) {
+      int key_lo, key_hi;
+      row_keys(p, w, qrow, key_lo, key_hi);
+      for (int j = 0, kb = w.j0 * kBN; j < n; ++j, kb += kBN) {
         if (!wait_bar_warp(bar_s, s_cnt & 1u, ctl)) return;
         ++s_cnt;
         ptx::tc_fence_after();
-        int limit = (p.causal && j == diag) ? row : 127;
-        limit = min(limit, w.Lk - j * kBN - 1);
+        const int lo = key_lo - kb;
+        const int limit = min(kBN - 1, key_hi - kb);
         // the S(j) commit implies O += P(j-1) V(j-1) is done: no extra wait
-        softmax_step_pv<D, BF16>(tS, tO, limit, p.scale_log2, p.scale_pos != 0, j == 0, rs, 0u,
+        softmax_step_pv<D, BF16>(tS, tO, lo, limit, p.scale_log2, p.scale_pos != 0, j == 0, rs, 0u,
                                  0u, ctl);
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar_p);
@@ -540,7 +583,7 @@ __device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bars, cons
     for (int j = 0; j < nmax; ++j) {
       const uint32_t it = kv_it + j;
       const uint32_t st = it % NS;
-      const int krow = w.k_start + j * kBN;
+      const int krow = w.k_start + (w.j0 + j) * kBN;
       if (it >= NS && !wait_bar(bar(L::KE + st), (it / NS - 1) & 1u, ctl)) return;
       ptx::mbar_arrive_expect_tx(bar(L::KF + st), L::kTileBytes);
 #pragma unroll

@@ -107,7 +107,12 @@ __device__ __forceinline__ bool decode_pair(const FwdParams& p, int k, Cursor& c
   const int g = static_cast<int>(gridDim.x) / 2;
   const int cl = static_cast<int>(blockIdx.x) / 2;
   if (!decode_rows<kUR>(p, unit_of(k, g, cl), c, w, report)) return false;
-  n = max(tiles_for(p, w, q0_of(w, 0)), tiles_for(p, w, q0_of(w, 1)));
+  int lo0, hi0, lo1, hi1;
+  tile_keys(p, w, q0_of(w, 0), lo0, hi0);
+  tile_keys(p, w, q0_of(w, 1), lo1, hi1);
+  // the pair shares every K/V tile: from the even CTA's first to the last either needs
+  w.j0 = lo0;
+  n = max(0, max(hi0, hi1) - lo0);
   return true;
 }
 
@@ -118,9 +123,11 @@ __device__ __forceinline__ bool decode_pair(const FwdParams& p, int k, Cursor& c
 // halves exchange their partial maxima through shared memory at a named
 // barrier, so both take the same running max and rescale decisions; each
 // writes its 32 columns of P and rescales its 64 columns of O.  Masking: keys
-// c of this half with c > limit are invisible (limit already local to the half).
+// c of this half with c < lo or c > limit are invisible (both already local to
+// the half).
 template <bool BF16>
-__device__ __forceinline__ bool softmax_half_step(uint32_t tS, uint32_t tP, uint32_t tO, int limit,
+__device__ __forceinline__ bool softmax_half_step(uint32_t tS, uint32_t tP, uint32_t tO, int lo,
+                                                  int limit,
                                                   float cl, bool scale_pos, bool first,
                                                   RowState& st, float* x_mine,
                                                   const float* x_other, uint32_t bar_id,
@@ -134,10 +141,10 @@ __device__ __forceinline__ bool softmax_half_step(uint32_t tS, uint32_t tP, uint
     for (int c = 0; c < 64; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * cl);
     cle = 1.0f;
   }
-  if (limit < 63) {
+  if (limit < 63 || lo > 0) {
 #pragma unroll
     for (int c = 0; c < 64; ++c)
-      if (c > limit) r[c] = __float_as_uint(-INFINITY);
+      if (c > limit || c < lo) r[c] = __float_as_uint(-INFINITY);
   }
   float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
@@ -249,18 +256,22 @@ __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, u
                                : (static_cast<long long>(w.b) * p.H + w.h) * p.Sq + qrow;
     RowState rs{-INFINITY, 0.0f, 0.0f};
     if (n > 0) {
-      for (int j = 0; j < n; ++j) {
+      int key_lo, key_hi;  // visible keys of this row, shifted to this half's columns
+      row_keys(p, w, qrow, key_lo, key_hi);
+      key_lo -= 64 * half;
+      key_hi -= 64 * half;
+      for (int j = 0, kb = w.j0 * kBN; j < n; ++j, kb += kBN) {
         const uint32_t G = g_base + j;
         const uint32_t b = G % kNBuf;
         if (!wait_bar_warp(bars + 8 * (L::SF + b), (G / kNBuf) & 1u, ctl)) return;
         ptx::tc_fence_after();
-        int limit = p.causal ? min(127, qrow - j * kBN) : 127;
-        limit = min(limit, w.Lk - j * kBN - 1) - 64 * half;
+        const int lo = key_lo - kb;
+        const int limit = min(63, key_hi - kb);
         // O += P(G-1) V(G-1) may still be running: a rescale of O waits for it.
         const uint32_t gp = G - 1;
         float* const xm = xmax + (G & 1u) * 256;
         const uint32_t tSb = tmem + lane_bits + L::kColS + b * 128;
-        if (!softmax_half_step<BF16>(tSb + 64 * half, tSb + 32 * half, tO, limit, p.scale_log2,
+        if (!softmax_half_step<BF16>(tSb + 64 * half, tSb + 32 * half, tO, lo, limit, p.scale_log2,
                                      p.scale_pos != 0, j == 0, rs, xm + half * 128 + row,
                                      xm + (1 - half) * 128 + row, xbar,
                                      bars + 8 * (L::PVD + gp % kNBuf), (gp / kNBuf) & 1u, ctl))
@@ -427,7 +438,7 @@ static __device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bar
     for (int j = 0; j < n; ++j) {
       const uint32_t it = kv_it + j;
       const uint32_t st = it % NS;
-      const int krow = w.k_start + j * kBN;
+      const int krow = w.k_start + (w.j0 + j) * kBN;
       if (it >= NS && !wait_bar(bar(L::KE + st), (it / NS - 1) & 1u, ctl)) return;
       if (lead) ptx::mbar_arrive_expect_tx(bar(L::KF + st), 2 * L::kKHalf);
 #pragma unroll

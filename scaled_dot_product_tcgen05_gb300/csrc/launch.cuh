@@ -17,6 +17,23 @@ extern template cudaError_t launch_fwd_2sm<false>(const FwdParams&, int, cudaStr
 extern template cudaError_t launch_fwd_2sm<true>(const FwdParams&, int, cudaStream_t);
 }  // namespace pair
 
+// Fills the visibility fields of `p` (see FwdParams) from the C arguments:
+// window_left / window_right = -1 leave that side unbounded, causal bounds the
+// right side at the diagonal, rows below global_q see all keys.  Returns false
+// for a request the rules reject (a negative size other than -1, or a right
+// window wider than 0 together with causal).
+inline bool set_mask(FwdParams& p, int causal, int window_left, int window_right, int global_q) {
+  if (window_left < -1 || window_right < -1 || global_q < 0) return false;
+  if (causal && window_right > 0) return false;
+  p.causal = causal ? 1 : 0;
+  p.win_left = window_left < 0 ? kUnbounded : (window_left < kUnbounded ? window_left : kUnbounded);
+  p.win_right = causal ? 0
+                       : (window_right < 0 ? kUnbounded
+                                           : (window_right < kUnbounded ? window_right : kUnbounded));
+  p.global_q = global_q;
+  return true;
+}
+
 struct LaunchInfo {
   int grid = 0;
   int smem = 0;

@@ -195,7 +195,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   p.Sq = Sq;
   p.Sk = Sk;
   p.varlen = varlen ? 1 : 0;
-  p.causal = causal ? 1 : 0;
+  set_mask(p, causal, -1, -1, 0);  // no window: cannot fail
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.scale_pos = scale > 0.0f ? 1 : 0;
   p.timeout_ns = 5000LL * 1000000LL;

@@ -43,6 +43,12 @@ class Workload:
     draw: int = 0
     varlen: bool = False
     len_range: tuple = (128, 4096)  # inclusive, varlen only
+    window: tuple = (-1, -1)        # (left, right) band of keys per query; -1 = unbounded
+    global_q: int = 0               # leading query rows that ignore the window
+
+    @property
+    def windowed(self) -> bool:
+        return tuple(self.window) != (-1, -1) or self.global_q != 0
 
     @property
     def base_seed(self) -> int:
@@ -67,6 +73,9 @@ def standard_workloads() -> dict:
                 draw 0: N(0,1) everywhere; draw 1: Q,K ~ N(0,16), V ~ N(0,1)
     4 varlen    16 sequences, lengths uniform in [128, 4096], H=32 D=128 bf16 causal
     5 long      B=1 H=32 S=65536 (and 131072) D=128 bf16 causal
+    6 window    B=1 H=32 S=131072 D=128 bf16 causal, sliding window of 4096 keys
+                (the query and the 4095 before it) with 64 global query rows: the
+                128K-context hybrid of page "长文本处理性能断层真相", §2.5
     """
     w = {}
     for c in (False, True):
@@ -81,6 +90,8 @@ def standard_workloads() -> dict:
                                   dtype="bf16", causal=True, varlen=True)
     w["long64k_causal"] = _wl("long64k_causal", 5, 1, 32, 65536, 128, "bf16", True)
     w["long128k_causal"] = _wl("long128k_causal", 5, 1, 32, 131072, 128, "bf16", True, draw=2)
+    w["window128k_causal"] = _wl("window128k_causal", 6, 1, 32, 131072, 128, "bf16", True,
+                                 window=(4095, 0), global_q=64)
     return w
 
 
@@ -170,3 +181,31 @@ def attention_flops(B: int, H: int, Sq: int, Sk: int, D: int, causal: bool) -> f
 def varlen_flops(lengths: Sequence[int], H: int, D: int, causal: bool) -> float:
     """Sum over sequences of attention_flops(1, H, L, L, D, causal)."""
     return sum(attention_flops(1, H, int(L), int(L), D, causal) for L in lengths)
+
+
+def visible_key_counts(Sq: int, Sk: int, causal: bool, window=(-1, -1), global_q: int = 0):
+    """Number of keys each query row 0..Sq-1 of one sequence may see (int64 array).
+
+    Used only to count the work of windowed problems (FLOPs = 4*D per visible
+    (query, key) pair); row i >= global_q sees keys max(0, i-left) ..
+    min(Sk-1, i+right), rows below global_q see all keys, causal caps at i.
+    """
+    import numpy as np
+    i = np.arange(Sq, dtype=np.int64)
+    wl, wr = window
+    lo = np.zeros(Sq, dtype=np.int64)
+    hi = np.full(Sq, Sk, dtype=np.int64)
+    band = i >= global_q
+    if wl >= 0:
+        lo = np.where(band, np.maximum(0, i - wl), lo)
+    if wr >= 0:
+        hi = np.where(band, np.minimum(Sk, i + wr + 1), hi)
+    if causal:
+        hi = np.minimum(hi, i + 1)
+    return np.maximum(0, hi - lo)
+
+
+def window_flops(B: int, H: int, Sq: int, Sk: int, D: int, causal: bool, window=(-1, -1),
+                 global_q: int = 0) -> float:
+    """4 * D FLOPs per visible (query, key) pair, summed over rows, heads and batch."""
+    return 4.0 * D * B * H * float(visible_key_counts(Sq, Sk, causal, window, global_q).sum())

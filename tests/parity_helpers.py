@@ -38,14 +38,15 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, row_mask=None, what=""):
     return stats
 
 
-def run_gpu(q, k, v, causal, scale, cu_q=None, cu_k=None, stream=None):
+def run_gpu(q, k, v, causal, scale, cu_q=None, cu_k=None, stream=None, window=(-1, -1),
+            global_q=0):
     """Copies host inputs to cuda:0, runs attn_fwd, checks the device status."""
     dev = torch.device("cuda:0")
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     cq = cu_q.to(dev) if cu_q is not None else None
     ck = cu_k.to(dev) if cu_k is not None else None
     o, lse = pkg.attn_fwd(qd, kd, vd, causal=causal, scale=scale, cu_seqlens_q=cq,
-                          cu_seqlens_k=ck, stream=stream)
+                          cu_seqlens_k=ck, stream=stream, window=window, global_q=global_q)
     st = pkg.attn_check(stream)
     assert st == pkg.ATTN_OK, pkg.status_string(st)
     return o, lse

@@ -121,3 +121,27 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp", ".c")):
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert not pat.search(text), f
+
+
+def call_window(lib, wl, wr, g, **kw):
+    args = dict(q=A, k=A + 0x100, v=A + 0x200, o=A + 0x300, lse=A + 0x400, B=1, H=2, Sq=128,
+                Sk=128, D=64, scale=0.125, causal=0, cq=0, ck=0, dtype=0)
+    args.update(kw)
+    return pkg.attn_fwd_window_raw(args["q"], args["k"], args["v"], args["o"], args["lse"],
+                                   args["B"], args["H"], args["Sq"], args["Sk"], args["D"],
+                                   args["scale"], args["causal"], wl, wr, g, args["cq"],
+                                   args["ck"], args["dtype"], 0)
+
+
+@pytest.mark.parametrize("wl,wr,g,causal", [
+    (-2, 0, 0, 0), (0, -2, 0, 0), (5, 5, -1, 0), (5, 1, 0, 1), (-1, 3, 0, 1),
+])
+def test_window_arguments_rejected_before_launch(lib, wl, wr, g, causal):
+    assert call_window(lib, wl, wr, g, causal=causal) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_window_entry_point_shares_attn_fwd_checks(lib):
+    assert call_window(lib, 4, 0, 0, causal=1, D=96) == pkg.ATTN_ERR_UNSUPPORTED
+    assert call_window(lib, 4, 0, 0, causal=1, q=A + 8) == pkg.ATTN_ERR_MISALIGNED
+    assert call_window(lib, 4, 0, 0, causal=1, B=0) == pkg.ATTN_OK
+    assert call_window(lib, -1, -1, 0, Sq=0) == pkg.ATTN_OK
