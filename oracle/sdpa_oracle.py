@@ -42,8 +42,9 @@ Readings where the pages are silent:
     W - 1, window_right = 0; the page's "full attention" for the global rows
     keeps the causal rule when the call is causal.
 
-Parity status: every function here is pinned by tests/test_oracle.py (brute
-force, closed forms, invariants, a library routine); none is "parity unpinned".
+Parity status: every function here is pinned (tests/test_oracle.py,
+tests/test_oracle_window.py, tests/test_oracle_decode.py: brute force, closed
+forms, invariants, a library routine); none is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -162,3 +163,72 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: 
             o[q0:q1, h, :] = ob
             lse[h, q0:q1] = lb
     return o, lse
+
+
+def attention_decode(q, k_cache, v_cache, seqlens_k, scale: float, causal: bool,
+                     heads: Optional[Sequence[int]] = None):
+    """Decode against a KV cache: the Sq new queries are the LAST Sq positions.
+
+    q [B,Sq,H,D], k_cache/v_cache [B,Sk,H,D], seqlens_k [B] (valid cache rows,
+    None = Sk).  Query t of sequence b sits at position L_b - Sq + t, so with
+    causal it sees keys 0 .. L_b - Sq + t (the KV-cache layout and decode step of
+    page "长文本处理性能断层真相", §2.2); without causal it sees keys 0 .. L_b-1.
+    Written as the top-left causal definition applied to a query array whose
+    rows L_b-Sq .. L_b-1 hold the new queries.  A query at a negative position
+    sees no key: O = 0, LSE = -inf.  Returns O [B,Sq,H,D], LSE [B,H,Sq].
+    """
+    q, kc, vc = _as_f64(q), _as_f64(k_cache), _as_f64(v_cache)
+    B, Sq, H, D = q.shape
+    Sk = kc.shape[1]
+    Dv = vc.shape[3]
+    lens = [Sk] * B if seqlens_k is None else [int(x) for x in np.asarray(seqlens_k).tolist()]
+    o = np.full((B, Sq, H, Dv), np.nan)
+    lse = np.full((B, H, Sq), np.nan)
+    for b in range(B):
+        L = lens[b]
+        for h in (range(H) if heads is None else heads):
+            o[b, :, h, :] = 0.0
+            lse[b, h, :] = -np.inf
+            if L == 0:
+                continue
+            if not causal:  # every new query sees the L cached keys
+                ob, lb = attention_one_head(q[b, :, h, :], kc[b, :L, h, :], vc[b, :L, h, :],
+                                            scale, False)
+                o[b, :, h, :], lse[b, h, :] = ob, lb
+                continue
+            # causal: query t at row L - Sq + t of a length-L query array
+            live = [t for t in range(Sq) if L - Sq + t >= 0]
+            if not live:
+                continue
+            qpos = np.zeros((L, D))
+            for t in live:
+                qpos[L - Sq + t] = q[b, t, h, :]
+            ob, lb = attention_one_head(qpos, kc[b, :L, h, :], vc[b, :L, h, :], scale, True,
+                                        rows=[L - Sq + t for t in live])
+            o[b, live, h, :] = ob
+            lse[b, h, live] = lb
+    return o, lse
+
+
+def merge_partials(o_parts, lse_parts):
+    """Combine attention results computed over disjoint key sets.
+
+    o_parts [P, ..., D], lse_parts [P, ...] (natural log).  With w_p =
+    exp(LSE_p - max_p LSE_p): O = sum_p w_p O_p / sum_p w_p and
+    LSE = max_p LSE_p + ln sum_p w_p -- the softmax over the union of the key
+    sets, rebuilt from per-set results (the combine step of the ring attention
+    on page "长文本处理性能断层真相", §1, where each GPU holds a slice of the
+    tokens).  Entries whose parts are all -inf give O = 0, LSE = -inf.
+    """
+    o = _as_f64(o_parts)
+    lp = _as_f64(lse_parts)
+    m = lp.max(axis=0)
+    finite = np.isfinite(m)
+    m_safe = np.where(finite, m, 0.0)
+    w = np.where(np.isneginf(lp), 0.0, np.exp(lp - m_safe[None]))
+    z = w.sum(axis=0)
+    out = (w[..., None] * o).sum(axis=0) / np.where(finite, z, 1.0)[..., None]
+    out = np.where(finite[..., None], out, 0.0)
+    with np.errstate(divide="ignore"):
+        lse = np.where(finite, m_safe + np.log(np.where(finite, z, 1.0)), -np.inf)
+    return out, lse
