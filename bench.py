@@ -17,6 +17,7 @@ value counts the work of all ranks.  Rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import re
@@ -35,6 +36,7 @@ from scaled_dot_product_tcgen05_gb300 import workloads as W  # noqa: E402
 DEFAULT_WORKLOAD = "long64k_causal"
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 FALLBACK_PEAK_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
 
 
 # ----------------------------------------------------------------------------- ranks
@@ -140,6 +142,14 @@ def peaks():
     return FALLBACK_PEAK_TFLOPS, "fallback (1.9 PFLOP/s bf16, earlier GB300 measurement)"
 
 
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy)"
+    return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
 def source_digest() -> str:
     import hashlib
     h = hashlib.sha256()
@@ -150,8 +160,10 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def kernel_name(D: int) -> str:
+def kernel_name(D: int, decode: bool = False) -> str:
     """The kernel attn_fwd launches (head dim 128 runs on CTA pairs unless ATTN_PAIR=0)."""
+    if decode:
+        return "attn_decode_kernel"
     return "attn_fwd_kernel_2sm" if D == 128 and os.environ.get("ATTN_PAIR") != "0" \
         else "attn_fwd_kernel"
 
@@ -170,6 +182,16 @@ def profiled_traffic(workload: str, kernel: str):
 
 
 def workload_info(wl):
+    if wl.decode:  # every cached K/V byte read once; q, o, lse
+        keys = W.visible_key_counts(wl.Sk, wl.Sk, wl.causal)[wl.Sk - wl.Sq:] if wl.causal \
+            else [wl.Sk] * wl.Sq
+        flops = 4.0 * wl.D * wl.B * wl.H * float(sum(int(x) for x in keys))
+        nbytes = (wl.B * wl.Sk * wl.H * wl.D * 2 * 2 + wl.B * wl.Sq * wl.H * wl.D * 2 * 2
+                  + wl.B * wl.H * wl.Sq * 4)
+        cfg = {"workload": wl.name, "B": wl.B, "H": wl.H, "Sq": wl.Sq, "Sk": wl.Sk, "D": wl.D,
+               "causal": wl.causal, "dtype": wl.dtype, "decode": True, "flops_per_step": flops,
+               "algorithmic_bytes_per_step": nbytes}
+        return flops, nbytes, cfg
     if wl.varlen:
         lens = W.varlen_lengths(wl).tolist()
         flops = W.varlen_flops(lens, wl.H, wl.D, wl.causal)
@@ -204,10 +226,44 @@ def _row_keys(wl, rows):
 
 
 # ------------------------------------------------------------------ reference (oracle)
+def _decode_oracle_sample(wl, n_heads):
+    """Inputs of the first n_heads heads of sequence 0 of a decode workload, and a
+    callable running the oracle on them; returns (run, cache bytes, flops)."""
+    from oracle.sdpa_oracle import attention_decode
+    heads = list(range(min(n_heads, wl.H)))
+    inp = W.make_inputs(wl, heads=heads)
+    q, k, v = (inp[n][:1, :, heads].contiguous() for n in ("q", "k", "v"))
+    run = lambda: attention_decode(q, k, v, None, wl.scale, wl.causal)  # noqa: E731
+    per_head_flops, per_head_bytes, _ = workload_info(dataclasses.replace(wl, B=1, H=1))
+    return run, per_head_bytes * len(heads), per_head_flops * len(heads)
+
+
 def run_reference(args, wl, flops_full, cfg):
     """Times the fp64 CPU oracle, as it stands, on a bounded sample of the workload."""
     import numpy as np
     from oracle.sdpa_oracle import attention_one_head
+
+    if wl.decode:
+        run, nbytes, _ = _decode_oracle_sample(wl, 2)
+        for _ in range(args.warmup):
+            run()
+        times = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            run()
+            times.append(time.perf_counter() - t0)
+        t = sum(times) / len(times)
+        value = nbytes / t / 1e9
+        sample = f"sequence 0, heads 0-1 of {wl.name} ({nbytes:.3g} cache bytes per step)"
+        return {"metric": "attention decode GB/s", "value": value, "unit": "GB/s",
+                "impl": "reference", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": cfg,
+                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_threads(),
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
 
     heads = list(range(min(2, wl.H)))
     S = wl.Sq
@@ -262,6 +318,19 @@ def cpu_baseline_sample(wl, budget_s: float):
     """The oracle on a bounded sample of the same workload (rank 0 only)."""
     import numpy as np
     from oracle.sdpa_oracle import attention_one_head
+
+    if wl.decode:  # head 0 of sequence 0, repeated until the budget is spent
+        run, nbytes, _ = _decode_oracle_sample(wl, 1)
+        spent, n = 0.0, 0
+        while spent < budget_s and n < 10000:
+            t0 = time.perf_counter()
+            run()
+            spent += time.perf_counter() - t0
+            n += 1
+        return {"value": n * nbytes / spent / 1e9, "unit": "GB/s", "cores": cpu_threads(),
+                "kind": "oracle",
+                "sample": f"head 0 of sequence 0 of {wl.name}, {n} runs, "
+                          f"{spent:.1f} s of fp64 numpy work"}
 
     inp = W.make_inputs(wl, heads=[0]) if not wl.varlen else None
     if inp is None:
@@ -330,9 +399,17 @@ def main(argv=None):
         o = torch.empty_like(q)
         lse_shape = (wl.H, q.shape[0]) if wl.varlen else (wl.B, wl.H, wl.Sq)
         lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+        ws_dec = None
+        if wl.decode:
+            need = pkg.decode_workspace_bytes(wl.B, wl.H, wl.Sq, wl.Sk, wl.D)
+            ws_dec = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
     def step():
+        if wl.decode:
+            pkg.attn_decode(q, k, v, causal=wl.causal, scale=wl.scale, workspace=ws_dec, out=o,
+                            lse=lse, stream=stream)
+            return
         pkg.attn_fwd(q, k, v, causal=wl.causal, scale=wl.scale, cu_seqlens_q=cu,
                      cu_seqlens_k=cu, out=o, lse=lse, window=wl.window, global_q=wl.global_q,
                      stream=stream)
@@ -344,6 +421,9 @@ def main(argv=None):
     if st != pkg.ATTN_OK:
         raise SystemExit(f"device status {pkg.status_string(st)}")
     grid, smem = pkg.last_launch()
+    launches_per_step = 1
+    if wl.decode and pkg.decode_workspace_bytes(wl.B, wl.H, wl.Sq, wl.Sk, wl.D) > 0:
+        launches_per_step = 2  # the split decode kernel and the merge kernel
     sampler = ClockSampler(local)
     sampler.start()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -397,9 +477,18 @@ def main(argv=None):
 
     if rank != 0:
         return 0
-    peak, peak_src = peaks()
-    achieved = flops / (kernel_ms * 1e-3) / 1e12
-    kern = kernel_name(wl.D)
+    if wl.decode:  # HBM-bound: bytes per step against the measured copy bandwidth
+        peak, peak_src = hbm_peak()
+        achieved = nbytes / (kernel_ms * 1e-3) / 1e9
+        kern = kernel_name(wl.D, decode=True)
+        per_step = nbytes * ws / 1e9
+        unit, metric, bound = "GB/s", "attention decode GB/s", "hbm"
+    else:
+        peak, peak_src = peaks()
+        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        kern = kernel_name(wl.D)
+        per_step = flops * ws / 1e12
+        unit, metric, bound = "TFLOP/s", "attention fwd TFLOP/s", "tensor"
     traffic = profiled_traffic(wl.name, kern)
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
@@ -408,18 +497,18 @@ def main(argv=None):
                l2="no flush: inputs %.2f GiB > 129 MB L2" % (h2d / 2 ** 30),
                grid_ctas=grid, smem_bytes=smem)
     out = {
-        "metric": "attention fwd TFLOP/s", "value": flops * ws / (ms_step * 1e-3) / 1e12,
-        "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "metric": metric, "value": per_step / (ms_step * 1e-3),
+        "unit": unit, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "fp16",
         "data": "synthetic", "config": cfg,
         "pct_of_peak": achieved / peak,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                      "kernel": kern, "kernel_ms": kernel_ms},
-        "e2e": {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": per_step / (e2e_ms * 1e-3), "unit": unit,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
         "cpu_baseline": cpu,
     }

@@ -20,6 +20,7 @@
 #ifndef ATTN_TCGEN05_H
 #define ATTN_TCGEN05_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -105,6 +106,64 @@ int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float*
                     int window_left, int window_right, int global_q,
                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
                     int dtype, void* stream);
+
+/*
+ * attn_fwd_decode -- attention of a few new queries against a KV cache.
+ *
+ * Decode step of page "长文本处理性能断层真相" (lnrk.cn), §2.2: the cache holds
+ * the keys/values of every earlier token and grows with the sequence; the Sq
+ * new queries of sequence b are the last Sq positions, L_b - Sq .. L_b - 1, of
+ * a sequence whose cache holds L_b rows.  Key j of the cache is visible to new
+ * query t when j < L_b and, if causal, j <= L_b - Sq + t (queries at negative
+ * positions see nothing: O = 0, LSE = -inf).  The keys are split into chunks
+ * processed in parallel and the partial results are combined with the
+ * log-sum-exp merge of attn_merge (the ring-attention combine step of the same
+ * page, §1), so one sequence can use the whole GPU.
+ *
+ * Layouts (row-major, contiguous, head dim innermost):
+ *   q, o              [B, Sq, H, D]       fp16/bf16 (per dtype)
+ *   k_cache, v_cache  [B, Sk, H, D]       Sk = cache capacity (rows per sequence)
+ *   lse               float [B, H, Sq]    natural log, like attn_fwd
+ *   seqlens_k         int32 [B] on the device: valid rows L_b (0 <= L_b <= Sk),
+ *                     or NULL for L_b = Sk.  A value outside [0, Sk] sets the
+ *                     device error word (ATTN_ERR_BAD_SEQLENS via attn_check).
+ * Arguments: 1 <= Sq <= 16 (else ATTN_ERR_UNSUPPORTED), D 64 or 128, finite
+ * scale; q, k_cache, v_cache, o 16-byte aligned, lse and seqlens_k 4-byte.
+ * workspace: device scratch of at least the size attn_decode_workspace reports
+ * for the same B, H, Sq, Sk, D on the current device (256-byte aligned; may be
+ * NULL when that size is 0).  The caller owns it and must not use it for
+ * anything else until the call's work on `stream` has finished.
+ * Errors and ownership as attn_fwd; asynchronous on `stream`.
+ */
+int attn_fwd_decode(const void* q, const void* k_cache, const void* v_cache, void* o,
+                    float* lse, int B, int H, int Sq, int Sk, int D, float scale, int causal,
+                    const int32_t* seqlens_k, void* workspace, size_t workspace_bytes,
+                    int dtype, void* stream);
+
+/*
+ * attn_decode_workspace -- bytes of workspace attn_fwd_decode needs for these
+ * sizes on the current device (0 when the keys are not split).  Same argument
+ * rules as attn_fwd_decode; the value depends on the device's SM count.
+ */
+int attn_decode_workspace(int B, int H, int Sq, int Sk, int D, size_t* bytes);
+
+/*
+ * attn_merge -- combine attention results computed over disjoint key sets.
+ *
+ * For n_parts results of the same queries over disjoint key sets (for example
+ * the shards of a ring attention, page "长文本处理性能断层真相", §1, or the
+ * key chunks of a long sequence), returns attention over the union:
+ *   w_p = exp(LSE_p - max_p LSE_p),  O = sum_p w_p O_p / sum_p w_p,
+ *   LSE = max_p LSE_p + ln sum_p w_p;   rows where every LSE_p is -inf get
+ *   O = 0 and LSE = -inf.
+ * Layouts: o_parts [n_parts, B, S, H, D] (dtype), lse_parts float
+ * [n_parts, B, H, S] -- the outputs of n_parts attn_fwd calls stacked (a varlen
+ * result is B = 1, S = total rows); o [B, S, H, D] (dtype), lse float [B, H, S].
+ * n_parts >= 1, any D >= 1; 2-byte (o) and 4-byte (lse) alignment.
+ * Errors and ownership as attn_fwd; asynchronous on `stream`.
+ */
+int attn_merge(const void* o_parts, const float* lse_parts, int n_parts, int B, int S, int H,
+               int D, void* o, float* lse, int dtype, void* stream);
 
 /*
  * attn_check -- synchronise `stream`, then report and clear the device error

@@ -15,9 +15,12 @@ from ._binding import (  # noqa: F401
     EXPORTED,
     AttnError,
     attn_check,
+    attn_decode,
     attn_fwd,
     attn_fwd_raw,
     attn_fwd_window_raw,
+    attn_merge,
+    decode_workspace_bytes,
     last_launch,
     load_library,
     num_sms,

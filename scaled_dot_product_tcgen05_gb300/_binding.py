@@ -28,7 +28,8 @@ ATTN_ERR_BAD_SEQLENS = -6
 DTYPE_CODES = {torch.float16: 0, torch.bfloat16: 1}
 
 EXPORTED = ("attn_fwd", "attn_check", "attn_status_string", "attn_num_sms",
-            "attn_last_launch", "attn_release", "attn_fwd_noalloc", "attn_fwd_window")
+            "attn_last_launch", "attn_release", "attn_fwd_noalloc", "attn_fwd_window",
+            "attn_fwd_decode", "attn_decode_workspace", "attn_merge")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -59,6 +60,13 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.attn_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i, i, vp, vp,
                                         i, vp]
         lib.attn_fwd_window.restype = i
+        lib.attn_fwd_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp,
+                                        ctypes.c_size_t, i, vp]
+        lib.attn_fwd_decode.restype = i
+        lib.attn_decode_workspace.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_decode_workspace.restype = i
+        lib.attn_merge.argtypes = [vp, vp, i, i, i, i, i, vp, vp, i, vp]
+        lib.attn_merge.restype = i
         lib.attn_check.argtypes = [vp]
         lib.attn_check.restype = i
         lib.attn_status_string.argtypes = [i]
@@ -187,6 +195,99 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool 
                               DTYPE_CODES[q.dtype], _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_window" if windowed else "attn_fwd")
+    return out, lse
+
+
+def _check_16bit(name, t):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in DTYPE_CODES:
+        raise ValueError(f"{name} must be fp16 or bf16, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def decode_workspace_bytes(B: int, H: int, Sq: int, Sk: int, D: int) -> int:
+    """Workspace bytes attn_fwd_decode needs for these sizes on the current device."""
+    n = ctypes.c_size_t(0)
+    st = load_library().attn_decode_workspace(B, H, Sq, Sk, D, ctypes.byref(n))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_decode_workspace")
+    return int(n.value)
+
+
+def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, *,
+                seqlens_k: Optional[torch.Tensor] = None, causal: bool = True,
+                scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None,
+                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Attention of Sq <= 16 new queries per sequence against a KV cache.
+
+    q [B,Sq,H,D], k_cache/v_cache [B,Sk,H,D], optional int32 seqlens_k [B] (valid
+    cache rows, default Sk).  The new queries are the last Sq positions of each
+    sequence; with ``causal`` query t sees cache rows 0 .. L_b - Sq + t.  Returns
+    (O [B,Sq,H,D], LSE fp32 [B,H,Sq]).  ``workspace`` (a CUDA uint8 tensor of at
+    least :func:`decode_workspace_bytes`) is allocated when not given.
+    """
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _check_16bit(name, t)
+    if not (q.dtype == k_cache.dtype == v_cache.dtype):
+        raise ValueError("q, k_cache, v_cache must share one dtype")
+    if q.dim() != 4 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("q must be [B,Sq,H,D] and k_cache/v_cache [B,Sk,H,D]")
+    B, Sq, H, D = q.shape
+    Sk = k_cache.shape[1]
+    if k_cache.shape != (B, Sk, H, D):
+        raise ValueError("k_cache/v_cache shape mismatch")
+    if seqlens_k is not None and (seqlens_k.dtype != torch.int32 or not seqlens_k.is_cuda or
+                                  seqlens_k.shape != (B,) or not seqlens_k.is_contiguous()):
+        raise ValueError("seqlens_k must be a contiguous int32 CUDA vector of B entries")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        need = decode_workspace_bytes(B, H, Sq, Sk, D)
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+        st = load_library().attn_fwd_decode(
+            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+            lse.data_ptr(), B, H, Sq, Sk, D, ctypes.c_float(scale), 1 if causal else 0,
+            seqlens_k.data_ptr() if seqlens_k is not None else None,
+            workspace.data_ptr() if need > 0 else None, workspace.numel(),
+            DTYPE_CODES[q.dtype], _stream_handle(stream) or None)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_decode")
+    return out, lse
+
+
+def attn_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, *,
+               out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+               stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Attention over the union of disjoint key sets from per-set results.
+
+    o_parts [P,B,S,H,D] (fp16/bf16), lse_parts fp32 [P,B,H,S] (stacked attn_fwd
+    outputs; a varlen result is B = 1) -> (O [B,S,H,D], LSE [B,H,S]).
+    """
+    _check_16bit("o_parts", o_parts)
+    if o_parts.dim() != 5:
+        raise ValueError("o_parts must be [P, B, S, H, D]")
+    P, B, S, H, D = o_parts.shape
+    if (lse_parts.shape != (P, B, H, S) or lse_parts.dtype != torch.float32 or
+            not lse_parts.is_cuda or not lse_parts.is_contiguous()):
+        raise ValueError("lse_parts must be a contiguous fp32 CUDA tensor [P, B, H, S]")
+    if out is None:
+        out = torch.empty(o_parts.shape[1:], dtype=o_parts.dtype, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=o_parts.device)
+    with torch.cuda.device(o_parts.device):
+        st = load_library().attn_merge(o_parts.data_ptr(), lse_parts.data_ptr(), P, B, S, H, D,
+                                       out.data_ptr(), lse.data_ptr(),
+                                       DTYPE_CODES[o_parts.dtype], _stream_handle(stream) or None)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_merge")
     return out, lse
 
 

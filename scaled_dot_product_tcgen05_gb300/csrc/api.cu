@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "attn.h"
+#include "decode_kernel.cuh"
 #include "launch.cuh"
 
 namespace attn {
@@ -207,6 +208,206 @@ extern "C" int attn_fwd_window(const void* q, const void* k, const void* v, void
                                int dtype, void* stream) {
   return fwd_impl(q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, window_left, window_right,
                   global_q, cu_seqlens_q, cu_seqlens_k, dtype, stream);
+}
+
+// ------------------------------------------------------------------ decode
+namespace attn {
+namespace dec {
+#define ATTN_DEC_EXTERN(D)                                                                   \
+  extern template cudaError_t launch_decode<D, 1, false>(const DecParams&, int, cudaStream_t); \
+  extern template cudaError_t launch_decode<D, 4, false>(const DecParams&, int, cudaStream_t); \
+  extern template cudaError_t launch_decode<D, 16, false>(const DecParams&, int, cudaStream_t); \
+  extern template cudaError_t launch_decode<D, 1, true>(const DecParams&, int, cudaStream_t);  \
+  extern template cudaError_t launch_decode<D, 4, true>(const DecParams&, int, cudaStream_t);  \
+  extern template cudaError_t launch_decode<D, 16, true>(const DecParams&, int, cudaStream_t);
+ATTN_DEC_EXTERN(64)
+ATTN_DEC_EXTERN(128)
+#undef ATTN_DEC_EXTERN
+extern template cudaError_t launch_merge<float, false>(const float*, const float*, int, int, int,
+                                                       int, int, void*, float*, cudaStream_t);
+extern template cudaError_t launch_merge<float, true>(const float*, const float*, int, int, int,
+                                                      int, int, void*, float*, cudaStream_t);
+extern template cudaError_t launch_merge<uint16_t, false>(const uint16_t*, const float*, int, int,
+                                                          int, int, int, void*, float*,
+                                                          cudaStream_t);
+extern template cudaError_t launch_merge<uint16_t, true>(const uint16_t*, const float*, int, int,
+                                                         int, int, int, void*, float*,
+                                                         cudaStream_t);
+}  // namespace dec
+
+namespace {
+
+// Split of the cache keys: about 8 units (sequence, head, chunk) per SM so the
+// persistent grid stays balanced, chunks of at least 256 keys (4 tiles).
+void decode_plan(int B, int H, int Sk, int sms, int* splits, int* chunk) {
+  const long long tiles = (static_cast<long long>(Sk) + dec::kKeys - 1) / dec::kKeys;
+  const long long bh = static_cast<long long>(B) * H;
+  long long want = (8LL * sms + bh - 1) / bh;
+  if (want > tiles) want = tiles;
+  if (want < 1) want = 1;
+  long long ct = (tiles + want - 1) / want;
+  const long long min_ct = tiles < 4 ? tiles : 4;
+  if (ct < min_ct) ct = min_ct;
+  if (ct < 1) ct = 1;
+  *chunk = static_cast<int>(ct * dec::kKeys);
+  *splits = static_cast<int>((tiles + ct - 1) / ct);
+}
+
+long long decode_ws_bytes(int B, int H, int Sq, int D, int splits) {
+  if (splits <= 1) return 0;
+  const long long o = static_cast<long long>(splits) * B * Sq * H * D * 4;
+  const long long l = static_cast<long long>(splits) * B * H * Sq * 4;
+  return ((o + 255) / 256) * 256 + l;
+}
+
+int current_device_state(DeviceState** ds) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  return device_state(dev, ds);
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" int attn_decode_workspace(int B, int H, int Sq, int Sk, int D, size_t* bytes) {
+  if (!bytes) return ATTN_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (B < 0 || H < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_INVALID_ARG;
+  if ((D != 64 && D != 128) || Sq > dec::kMaxSq) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0) return ATTN_OK;
+  DeviceState* ds = nullptr;
+  const int st = current_device_state(&ds);
+  if (st != ATTN_OK) return st;
+  int splits = 1, chunk = 0;
+  decode_plan(B, H, Sk, ds->sms, &splits, &chunk);
+  *bytes = static_cast<size_t>(decode_ws_bytes(B, H, Sq, D, splits));
+  return ATTN_OK;
+}
+
+extern "C" int attn_fwd_decode(const void* q, const void* k_cache, const void* v_cache, void* o,
+                               float* lse, int B, int H, int Sq, int Sk, int D, float scale,
+                               int causal, const int32_t* seqlens_k, void* workspace,
+                               size_t workspace_bytes, int dtype, void* stream) {
+  // ---- argument checks (no CUDA call before these pass)
+  if (B < 0 || H < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (Sq > dec::kMaxSq) return ATTN_ERR_UNSUPPORTED;
+  if (dtype != ATTN_DTYPE_FP16 && dtype != ATTN_DTYPE_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0) return ATTN_OK;
+  if (!q || !k_cache || !v_cache || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || (seqlens_k && !aligned(seqlens_k, 4)) ||
+      (workspace && !aligned(workspace, 256)))
+    return ATTN_ERR_MISALIGNED;
+  const long long rows_k = static_cast<long long>(B) * Sk;
+  if (rows_k > INT_MAX - 2 * dec::kKeys) return ATTN_ERR_INVALID_ARG;
+
+  // ---- device checks
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  DeviceState* ds = nullptr;
+  int st = device_state(dev, &ds);
+  if (st != ATTN_OK) return st;
+  int splits = 1, chunk = 0;
+  decode_plan(B, H, Sk, ds->sms, &splits, &chunk);
+  const long long units = static_cast<long long>(B) * H * splits;
+  if (units > INT_MAX / 2) return ATTN_ERR_INVALID_ARG;
+  const long long need = decode_ws_bytes(B, H, Sq, D, splits);
+  if (need > 0 && (!workspace || static_cast<long long>(workspace_bytes) < need))
+    return ATTN_ERR_INVALID_ARG;
+  if (!on_device(q, dev) || !on_device(k_cache, dev) || !on_device(v_cache, dev) ||
+      !on_device(o, dev) || !on_device(lse, dev) || (seqlens_k && !on_device(seqlens_k, dev)) ||
+      (need > 0 && !on_device(workspace, dev)))
+    return ATTN_ERR_INVALID_ARG;
+
+  // ---- parameters
+  dec::DecParams p;
+  const bool bf16 = dtype == ATTN_DTYPE_BF16;
+  if (encode_rows_heads_dim(&p.tm_k, k_cache, rows_k, H, D, bf16, dec::kKeys) != ATTN_OK ||
+      encode_rows_heads_dim(&p.tm_v, v_cache, rows_k, H, D, bf16, dec::kKeys) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+  p.q = static_cast<const uint16_t*>(q);
+  p.o = o;
+  p.lse = lse;
+  p.seqlens = seqlens_k;
+  float* ws = static_cast<float*>(workspace);
+  p.ws_o = need > 0 ? ws : nullptr;
+  p.ws_lse = need > 0 ? ws + ((static_cast<long long>(splits) * B * Sq * H * D * 4 + 255) / 256) *
+                                 64
+                      : nullptr;
+  p.err = ds->err;
+  p.B = B;
+  p.H = H;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.splits = splits;
+  p.chunk = chunk;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.timeout_ns = timeout_ns_from_env();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int grid = static_cast<int>(units < ds->sms ? units : ds->sms);
+  cudaError_t e;
+#define ATTN_DEC_LAUNCH(DD, BB)                                                   \
+  (Sq == 1 ? dec::launch_decode<DD, 1, BB>(p, grid, s)                          \
+           : Sq <= 4 ? dec::launch_decode<DD, 4, BB>(p, grid, s)                \
+                     : dec::launch_decode<DD, 16, BB>(p, grid, s))
+  if (D == 64)
+    e = bf16 ? ATTN_DEC_LAUNCH(64, true) : ATTN_DEC_LAUNCH(64, false);
+  else
+    e = bf16 ? ATTN_DEC_LAUNCH(128, true) : ATTN_DEC_LAUNCH(128, false);
+#undef ATTN_DEC_LAUNCH
+  if (e == cudaSuccess && splits > 1)
+    e = bf16 ? dec::launch_merge<float, true>(p.ws_o, p.ws_lse, splits, B, Sq, H, D, o, lse, s)
+             : dec::launch_merge<float, false>(p.ws_o, p.ws_lse, splits, B, Sq, H, D, o, lse, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  t_last_grid = grid;
+  t_last_smem = D == 64 ? dec::DLayout<64>::kAlloc : dec::DLayout<128>::kAlloc;
+  return ATTN_OK;
+}
+
+extern "C" int attn_merge(const void* o_parts, const float* lse_parts, int n_parts, int B, int S,
+                          int H, int D, void* o, float* lse, int dtype, void* stream) {
+  if (n_parts < 1 || B < 0 || S < 0 || H < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_DTYPE_FP16 && dtype != ATTN_DTYPE_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || S == 0) return ATTN_OK;
+  if (!o_parts || !lse_parts || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(o_parts, 2) || !aligned(o, 2) || !aligned(lse_parts, 4) || !aligned(lse, 4))
+    return ATTN_ERR_MISALIGNED;
+  const long long rows = static_cast<long long>(B) * S * H;
+  if (rows * D > (1LL << 40) || rows / 4 + 1 > INT_MAX) return ATTN_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  DeviceState* ds = nullptr;
+  int st = device_state(dev, &ds);
+  if (st != ATTN_OK) return st;
+  if (!on_device(o_parts, dev) || !on_device(lse_parts, dev) || !on_device(o, dev) ||
+      !on_device(lse, dev))
+    return ATTN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint16_t* parts = static_cast<const uint16_t*>(o_parts);
+  const cudaError_t e =
+      dtype == ATTN_DTYPE_BF16
+          ? dec::launch_merge<uint16_t, true>(parts, lse_parts, n_parts, B, S, H, D, o, lse, s)
+          : dec::launch_merge<uint16_t, false>(parts, lse_parts, n_parts, B, S, H, D, o, lse, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
 }
 
 extern "C" int attn_check(void* stream) {

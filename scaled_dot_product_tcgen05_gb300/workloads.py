@@ -45,6 +45,7 @@ class Workload:
     len_range: tuple = (128, 4096)  # inclusive, varlen only
     window: tuple = (-1, -1)        # (left, right) band of keys per query; -1 = unbounded
     global_q: int = 0               # leading query rows that ignore the window
+    decode: bool = False            # Sq new queries against a full KV cache of Sk rows
 
     @property
     def windowed(self) -> bool:
@@ -76,6 +77,9 @@ def standard_workloads() -> dict:
     6 window    B=1 H=32 S=131072 D=128 bf16 causal, sliding window of 4096 keys
                 (the query and the 4095 before it) with 64 global query rows: the
                 128K-context hybrid of page "长文本处理性能断层真相", §2.5
+    7 decode    KV-cache decode (page "长文本处理性能断层真相", §2.2): one new token
+                per sequence against a 128K-token cache (B=1 H=32 D=128 bf16), and
+                a batch of 16 sequences with 32K-token caches and 4 new tokens each
     """
     w = {}
     for c in (False, True):
@@ -92,6 +96,11 @@ def standard_workloads() -> dict:
     w["long128k_causal"] = _wl("long128k_causal", 5, 1, 32, 131072, 128, "bf16", True, draw=2)
     w["window128k_causal"] = _wl("window128k_causal", 6, 1, 32, 131072, 128, "bf16", True,
                                  window=(4095, 0), global_q=64)
+    w["decode128k_q1"] = Workload(name="decode128k_q1", wid=7, B=1, H=32, Sq=1, Sk=131072,
+                                  D=128, dtype="bf16", causal=True, decode=True)
+    w["decode32k_b16_q4"] = Workload(name="decode32k_b16_q4", wid=7, B=16, H=32, Sq=4,
+                                     Sk=32768, D=128, dtype="bf16", causal=True, decode=True,
+                                     draw=1)
     return w
 
 
