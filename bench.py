@@ -150,13 +150,21 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
 
 
-def source_digest() -> str:
+# Sources each profiled kernel is compiled from (its device code and the helpers it uses).
+KERNEL_SOURCES = {
+    "attn_fwd_kernel_2sm": ("ptx.cuh", "fwd_kernel.cuh", "fwd_kernel_2sm.cuh"),
+    "attn_fwd_kernel": ("ptx.cuh", "fwd_kernel.cuh"),
+    "attn_decode_kernel": ("ptx.cuh", "fwd_kernel.cuh", "decode_kernel.cuh"),
+}
+
+
+def source_digest(kernel: str) -> str:
+    """Digest of the kernel's source files: a profile is valid only while it matches."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "scaled_dot_product_tcgen05_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -176,7 +184,7 @@ def profiled_traffic(workload: str, kernel: str):
     text = open(path).read()
     m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     m_h = re.search(r"source_digest:\s*([0-9a-f]+)", text)
-    if not (m_t and m_h) or m_h.group(1) != source_digest():
+    if not (m_t and m_h) or m_h.group(1) != source_digest(kernel):
         return None
     return float(m_t.group(1))
 

@@ -159,7 +159,8 @@ int attn_decode_workspace(int B, int H, int Sq, int Sk, int D, size_t* bytes);
  * Layouts: o_parts [n_parts, B, S, H, D] (dtype), lse_parts float
  * [n_parts, B, H, S] -- the outputs of n_parts attn_fwd calls stacked (a varlen
  * result is B = 1, S = total rows); o [B, S, H, D] (dtype), lse float [B, H, S].
- * n_parts >= 1, any D >= 1; 2-byte (o) and 4-byte (lse) alignment.
+ * n_parts >= 1; 1 <= D <= 1024 (else ATTN_ERR_UNSUPPORTED); B * S * H < 2^31;
+ * 2-byte (o) and 4-byte (lse) alignment.
  * Errors and ownership as attn_fwd; asynchronous on `stream`.
  */
 int attn_merge(const void* o_parts, const float* lse_parts, int n_parts, int B, int S, int H,

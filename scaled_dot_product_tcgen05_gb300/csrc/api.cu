@@ -16,6 +16,7 @@
 #include "attn.h"
 #include "decode_kernel.cuh"
 #include "launch.cuh"
+#include "merge_kernel.cuh"
 
 namespace attn {
 
@@ -237,20 +238,35 @@ extern template cudaError_t launch_merge<uint16_t, true>(const uint16_t*, const 
 
 namespace {
 
-// Split of the cache keys: about 8 units (sequence, head, chunk) per SM so the
-// persistent grid stays balanced, chunks of at least 256 keys (4 tiles).
+// Split of the cache keys into chunks of whole 64-key tiles.  Every CTA of the
+// persistent grid takes units round-robin, so the step lasts about
+// ceil(units / sms) chunks; the split count (from about 8 units per SM up to 4x
+// that) is the one whose busiest SM streams the fewest tiles relative to the
+// average, with chunks of at least 256 keys (4 tiles) where the cache allows.
 void decode_plan(int B, int H, int Sk, int sms, int* splits, int* chunk) {
   const long long tiles = (static_cast<long long>(Sk) + dec::kKeys - 1) / dec::kKeys;
   const long long bh = static_cast<long long>(B) * H;
   long long want = (8LL * sms + bh - 1) / bh;
   if (want > tiles) want = tiles;
   if (want < 1) want = 1;
-  long long ct = (tiles + want - 1) / want;
   const long long min_ct = tiles < 4 ? tiles : 4;
-  if (ct < min_ct) ct = min_ct;
-  if (ct < 1) ct = 1;
-  *chunk = static_cast<int>(ct * dec::kKeys);
-  *splits = static_cast<int>((tiles + ct - 1) / ct);
+  long long best_ct = 0;
+  double best_eff = -1.0;
+  for (long long s = want; s <= 4 * want && s <= tiles; ++s) {
+    long long ct = (tiles + s - 1) / s;
+    if (ct < min_ct) ct = min_ct;
+    const long long real = (tiles + ct - 1) / ct;
+    const long long units = bh * real;
+    const long long waves = (units + sms - 1) / sms;
+    const double eff = static_cast<double>(bh * tiles) / (static_cast<double>(sms) * waves * ct);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best_ct = ct;
+    }
+  }
+  if (best_ct < 1) best_ct = tiles < 1 ? 1 : tiles;
+  *chunk = static_cast<int>(best_ct * dec::kKeys);
+  *splits = static_cast<int>((tiles + best_ct - 1) / best_ct);
 }
 
 long long decode_ws_bytes(int B, int H, int Sq, int D, int splits) {
@@ -379,13 +395,14 @@ extern "C" int attn_fwd_decode(const void* q, const void* k_cache, const void* v
 extern "C" int attn_merge(const void* o_parts, const float* lse_parts, int n_parts, int B, int S,
                           int H, int D, void* o, float* lse, int dtype, void* stream) {
   if (n_parts < 1 || B < 0 || S < 0 || H < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
+  if (D > dec::kMergeMaxD) return ATTN_ERR_UNSUPPORTED;
   if (dtype != ATTN_DTYPE_FP16 && dtype != ATTN_DTYPE_BF16) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || S == 0) return ATTN_OK;
   if (!o_parts || !lse_parts || !o || !lse) return ATTN_ERR_INVALID_ARG;
   if (!aligned(o_parts, 2) || !aligned(o, 2) || !aligned(lse_parts, 4) || !aligned(lse, 4))
     return ATTN_ERR_MISALIGNED;
   const long long rows = static_cast<long long>(B) * S * H;
-  if (rows * D > (1LL << 40) || rows / 4 + 1 > INT_MAX) return ATTN_ERR_INVALID_ARG;
+  if (rows * D > (1LL << 40) || rows > INT_MAX) return ATTN_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();

@@ -1,6 +1,7 @@
 // Instantiation of the KV-cache decode kernel for head dim 64 (fp16 and bf16;
 // 1, up to 4 and up to 16 new queries per sequence) and of the merge kernel.
 #include "decode_kernel.cuh"
+#include "merge_kernel.cuh"
 
 namespace attn {
 namespace dec {

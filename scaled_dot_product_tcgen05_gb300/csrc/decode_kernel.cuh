@@ -354,57 +354,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
   }
 }
 
-// ------------------------------------------------------------------ merge
-// One warp per output row (b, t, h): O = sum_p w_p O_p / sum_p w_p with
-// w_p = exp(LSE_p - max LSE), LSE = max + ln sum_p w_p; all parts empty gives
-// O = 0, LSE = -inf.  Parts: o_parts [P, B, S, H, D] (fp32 or 16-bit),
-// lse_parts [P, B, H, S]; outputs o [B, S, H, D] (16-bit), lse [B, H, S].
-template <typename Tin, bool BF16>
-__global__ void __launch_bounds__(128) attn_merge_kernel(const Tin* __restrict__ o_parts,
-                                                         const float* __restrict__ lse_parts,
-                                                         int P, int B, int S, int H, int D,
-                                                         void* o, float* lse) {
-  const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
-  const long long rows = static_cast<long long>(B) * S * H;
-  if (row >= rows) return;
-  const int lane = threadIdx.x & 31;
-  const int h = static_cast<int>(row % H);
-  const long long bs = row / H;
-  const int s = static_cast<int>(bs % S);
-  const int b = static_cast<int>(bs / S);
-  const long long lrow = (static_cast<long long>(b) * H + h) * S + s;
-  const long long lstride = static_cast<long long>(B) * H * S;
-  const long long ostride = rows * D;
-  float M = -INFINITY;
-  for (int q = 0; q < P; ++q) M = fmaxf(M, lse_parts[q * lstride + lrow]);
-  float z = 0.0f;
-  if (M != -INFINITY)
-    for (int q = 0; q < P; ++q) z += __expf(lse_parts[q * lstride + lrow] - M);
-  uint16_t* const O = static_cast<uint16_t*>(o);
-  for (int d = lane; d < D; d += 32) {
-    float acc = 0.0f;
-    if (M != -INFINITY) {
-      for (int q = 0; q < P; ++q) {
-        const float lp = lse_parts[q * lstride + lrow];
-        if (lp == -INFINITY) continue;
-        float x;
-        if constexpr (sizeof(Tin) == 4) {
-          x = o_parts[q * ostride + row * D + d];
-        } else {
-          const uint16_t raw = reinterpret_cast<const uint16_t*>(o_parts)[q * ostride + row * D + d];
-          x = BF16 ? __uint_as_float(static_cast<uint32_t>(raw) << 16)
-                   : __half2float(__ushort_as_half(raw));
-        }
-        acc += __expf(lp - M) * x;
-      }
-      acc /= z;
-    }
-    O[row * D + d] = BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(acc))
-                          : __half_as_ushort(__float2half_rn(acc));
-  }
-  if (lane == 0) lse[lrow] = M == -INFINITY ? -INFINITY : M + __logf(z);
-}
-
 template <int D, int SQ, bool BF16>
 cudaError_t launch_decode(const DecParams& p, int grid, cudaStream_t stream) {
   const void* fn = reinterpret_cast<const void*>(&attn_decode_kernel<D, SQ, BF16>);
@@ -413,17 +362,6 @@ cudaError_t launch_decode(const DecParams& p, int grid, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<DecParams*>(&p)};
   return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, DLayout<D>::kAlloc, stream);
-}
-
-template <typename Tin, bool BF16>
-cudaError_t launch_merge(const Tin* o_parts, const float* lse_parts, int P, int B, int S, int H,
-                         int D, void* o, float* lse, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(B) * S * H;
-  const unsigned blocks = static_cast<unsigned>((rows + 3) / 4);
-  if (blocks == 0) return cudaSuccess;
-  attn_merge_kernel<Tin, BF16><<<blocks, 128, 0, stream>>>(o_parts, lse_parts, P, B, S, H, D, o,
-                                                           lse);
-  return cudaGetLastError();
 }
 
 }  // namespace dec
