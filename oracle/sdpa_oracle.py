@@ -232,3 +232,51 @@ def merge_partials(o_parts, lse_parts):
     with np.errstate(divide="ignore"):
         lse = np.where(finite, m_safe + np.log(np.where(finite, z, 1.0)), -np.inf)
     return out, lse
+
+
+def attention_backward_one_head(q, k, v, do, scale: float, causal: bool):
+    """Gradients of attention for one (sequence, head): returns dQ, dK, dV.
+
+    q [Sq, D], k [Sk, D], v [Sk, Dv], do = dL/dO [Sq, Dv], fp64.  The forward is
+    the same definition as attention_one_head (scores S = scale Q K^T, masked,
+    row softmax P, O = P V); the gradient is the chain rule through those three
+    steps.  Page "Multi-Head Attention的计算本质与性能瓶颈", §3.3, reserves the
+    backward interface (every operator implements backward(grad_output)) and
+    states that masked connections carry no gradient ("gradient mask"); it
+    gives no formulas, so this is plain calculus on the definition:
+        dV = P^T dO
+        dP = dO V^T
+        dS = P * (dP - rowsum(dP * P))        (softmax Jacobian, row by row)
+        dQ = scale * dS K,   dK = scale * dS^T Q
+    Masked entries have P = 0 and so no gradient; a row with no visible key
+    contributes nothing.
+    """
+    q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+    Sq, Sk = q.shape[0], k.shape[0]
+    _, _, p = attention_one_head(q, k, v, scale, causal, return_p=True)
+    dv = p.T @ do
+    dp = do @ v.T
+    row = (dp * p).sum(axis=1, keepdims=True)
+    ds = p * (dp - row)
+    dq = scale * (ds @ k)
+    dk = scale * (ds.T @ q)
+    return dq, dk, dv
+
+
+def attention_backward_dense(q, k, v, do, scale: float, causal: bool,
+                             heads: Optional[Sequence[int]] = None):
+    """Dense batch: q/do [B,Sq,H,D], k/v [B,Sk,H,D] -> dQ, dK, dV in the same layouts.
+
+    Heads not listed in ``heads`` are NaN.
+    """
+    q, k, v, do = (_as_f64(x) for x in (q, k, v, do))
+    B, Sq, H, D = q.shape
+    dq = np.full(q.shape, np.nan)
+    dk = np.full(k.shape, np.nan)
+    dv = np.full(v.shape, np.nan)
+    for b in range(B):
+        for h in (range(H) if heads is None else heads):
+            g = attention_backward_one_head(q[b, :, h], k[b, :, h], v[b, :, h], do[b, :, h],
+                                            scale, causal)
+            dq[b, :, h], dk[b, :, h], dv[b, :, h] = g
+    return dq, dk, dv
