@@ -155,6 +155,7 @@ KERNEL_SOURCES = {
     "attn_fwd_kernel_2sm": ("ptx.cuh", "fwd_kernel.cuh", "fwd_kernel_2sm.cuh"),
     "attn_fwd_kernel": ("ptx.cuh", "fwd_kernel.cuh"),
     "attn_decode_kernel": ("ptx.cuh", "fwd_kernel.cuh", "decode_kernel.cuh"),
+    "attn_bwd_kernel": ("ptx.cuh", "fwd_kernel.cuh", "bwd_kernel.cuh"),
 }
 
 
@@ -204,6 +205,9 @@ def workload_info(wl):
         lens = W.varlen_lengths(wl).tolist()
         flops = W.varlen_flops(lens, wl.H, wl.D, wl.causal)
         tokens = sum(lens)
+    elif wl.backward:  # five products of 2*Sq*Sk*D per head (S^T, dP^T, dV, dK, dQ)
+        flops = 2.5 * W.attention_flops(wl.B, wl.H, wl.Sq, wl.Sk, wl.D, wl.causal)
+        tokens = wl.B * wl.Sq
     elif wl.windowed:  # exact count of visible (query, key) pairs
         flops = W.window_flops(wl.B, wl.H, wl.Sq, wl.Sk, wl.D, wl.causal, wl.window, wl.global_q)
         tokens = wl.B * wl.Sq
@@ -211,15 +215,29 @@ def workload_info(wl):
         flops = W.attention_flops(wl.B, wl.H, wl.Sq, wl.Sk, wl.D, wl.causal)
         tokens = wl.B * wl.Sq
     elem = 2
-    # algorithmic bytes: read Q, K, V once, write O (16-bit) and LSE (fp32)
-    nbytes = tokens * wl.H * wl.D * elem * 4 + tokens * wl.H * 4
+    # algorithmic bytes: read Q, K, V once, write O (16-bit) and LSE (fp32);
+    # backward: read Q, K, V, O, dO and LSE, write dQ, dK, dV
+    n_tensors = 8 if wl.backward else 4
+    nbytes = tokens * wl.H * wl.D * elem * n_tensors + tokens * wl.H * 4
     cfg = {"workload": wl.name, "B": wl.B, "H": wl.H, "Sq": wl.Sq if not wl.varlen else tokens,
            "Sk": wl.Sk if not wl.varlen else tokens, "D": wl.D, "causal": wl.causal,
            "dtype": wl.dtype, "varlen": wl.varlen, "flops_per_step": flops,
            "algorithmic_bytes_per_step": nbytes}
     if wl.windowed:
         cfg.update(window=list(wl.window), global_q=wl.global_q)
+    if wl.backward:
+        cfg.update(backward=True)
     return flops, nbytes, cfg
+
+
+def _bwd_oracle_sample(wl, n_rows=2048):
+    """Head 0 of sequence 0, first n_rows positions (a causal prefix is itself a
+    complete causal problem); returns (run, flops)."""
+    from oracle.sdpa_oracle import attention_backward_one_head
+    inp = W.make_inputs(wl, heads=[0])
+    q, k, v, do = (inp[n][0, :n_rows, 0].double().numpy() for n in ("q", "k", "v", "do"))
+    run = lambda: attention_backward_one_head(q, k, v, do, wl.scale, wl.causal)  # noqa: E731
+    return run, 2.5 * W.attention_flops(1, 1, n_rows, n_rows, wl.D, wl.causal)
 
 
 def _mask_kw(wl):
@@ -251,6 +269,27 @@ def run_reference(args, wl, flops_full, cfg):
     import numpy as np
     from oracle.sdpa_oracle import attention_one_head
 
+    if wl.backward:
+        run, fl = _bwd_oracle_sample(wl)
+        for _ in range(args.warmup):
+            run()
+        times = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            run()
+            times.append(time.perf_counter() - t0)
+        t = sum(times) / len(times)
+        value = fl / t / 1e12
+        sample = f"head 0 of {wl.name}, first 2048 positions (a complete causal sub-problem)"
+        return {"metric": "attention bwd TFLOP/s", "value": value, "unit": "TFLOP/s",
+                "impl": "reference", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": cfg,
+                "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(),
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
     if wl.decode:
         run, nbytes, _ = _decode_oracle_sample(wl, 2)
         for _ in range(args.warmup):
@@ -327,6 +366,18 @@ def cpu_baseline_sample(wl, budget_s: float):
     import numpy as np
     from oracle.sdpa_oracle import attention_one_head
 
+    if wl.backward:  # a 2048-position causal prefix of head 0, repeated
+        run, fl = _bwd_oracle_sample(wl)
+        spent, n = 0.0, 0
+        while spent < budget_s and n < 1000:
+            t0 = time.perf_counter()
+            run()
+            spent += time.perf_counter() - t0
+            n += 1
+        return {"value": n * fl / spent / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
+                "kind": "oracle",
+                "sample": f"head 0, first 2048 positions of {wl.name}, {n} runs, "
+                          f"{spent:.1f} s of fp64 numpy work"}
     if wl.decode:  # head 0 of sequence 0, repeated until the budget is spent
         run, nbytes, _ = _decode_oracle_sample(wl, 1)
         spent, n = 0.0, 0
@@ -399,6 +450,7 @@ def main(argv=None):
 
     inp = W.make_inputs(wl, pin=True)
     q_h, k_h, v_h = inp["q"], inp["k"], inp["v"]
+    do_h = inp.get("do")
     cu_h = inp["cu_seqlens_q"]
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -411,9 +463,20 @@ def main(argv=None):
         if wl.decode:
             need = pkg.decode_workspace_bytes(wl.B, wl.H, wl.Sq, wl.Sk, wl.D)
             ws_dec = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        if wl.backward:  # O and LSE of the forward, computed once outside the timing
+            dout = do_h.to(dev, non_blocking=True)
+            pkg.attn_fwd(q, k, v, causal=wl.causal, scale=wl.scale, out=o, lse=lse,
+                         stream=stream)
+            ws_bwd = torch.empty(pkg.bwd_workspace_bytes(wl.B, wl.H, wl.Sq, wl.D),
+                                 dtype=torch.uint8, device=dev)
+            dq_t, dk_t, dv_t = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     torch.cuda.synchronize()
 
     def step():
+        if wl.backward:
+            pkg.attn_bwd(q, k, v, o, dout, lse, causal=wl.causal, scale=wl.scale,
+                         workspace=ws_bwd, dq=dq_t, dk=dk_t, dv=dv_t, stream=stream)
+            return
         if wl.decode:
             pkg.attn_decode(q, k, v, causal=wl.causal, scale=wl.scale, workspace=ws_dec, out=o,
                             lse=lse, stream=stream)
@@ -429,7 +492,7 @@ def main(argv=None):
     if st != pkg.ATTN_OK:
         raise SystemExit(f"device status {pkg.status_string(st)}")
     grid, smem = pkg.last_launch()
-    launches_per_step = 1
+    launches_per_step = 3 if wl.backward else 1  # backward: D pre-pass, main, dQ conversion
     if wl.decode and pkg.decode_workspace_bytes(wl.B, wl.H, wl.Sq, wl.Sk, wl.D) > 0:
         launches_per_step = 2  # the split decode kernel and the merge kernel
     sampler = ClockSampler(local)
@@ -456,12 +519,26 @@ def main(argv=None):
     # ---- end to end through the public API, host buffers, copies inside the region
     o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
     lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    if wl.backward:  # inputs q, k, v, o, dO, LSE in; dQ, dK, dV out
+        with torch.cuda.stream(stream):
+            o_h.copy_(o, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+        torch.cuda.synchronize()
+        g_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq_t, dk_t, dv_t)]
 
     def e2e_step():
         with torch.cuda.stream(stream):
             q.copy_(q_h, non_blocking=True)
             k.copy_(k_h, non_blocking=True)
             v.copy_(v_h, non_blocking=True)
+            if wl.backward:
+                o.copy_(o_h, non_blocking=True)
+                lse.copy_(lse_h, non_blocking=True)
+                dout.copy_(do_h, non_blocking=True)
+                step()
+                for hbuf, dbuf in zip(g_h, (dq_t, dk_t, dv_t)):
+                    hbuf.copy_(dbuf, non_blocking=True)
+                return
             step()
             o_h.copy_(o, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
@@ -482,6 +559,11 @@ def main(argv=None):
         raise SystemExit("non-finite output")
     h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * q_h.element_size()
     d2h = o_h.numel() * o_h.element_size() + lse_h.numel() * 4
+    if wl.backward:
+        h2d += (o_h.numel() + do_h.numel()) * q_h.element_size() + lse_h.numel() * 4
+        d2h = sum(t.numel() for t in g_h) * q_h.element_size()
+        if not all(torch.isfinite(t.float()).all() for t in g_h):
+            raise SystemExit("non-finite gradient")
 
     if rank != 0:
         return 0
@@ -497,6 +579,9 @@ def main(argv=None):
         kern = kernel_name(wl.D)
         per_step = flops * ws / 1e12
         unit, metric, bound = "TFLOP/s", "attention fwd TFLOP/s", "tensor"
+        if wl.backward:
+            kern = "attn_bwd_kernel"
+            metric = "attention bwd TFLOP/s"
     traffic = profiled_traffic(wl.name, kern)
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:

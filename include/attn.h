@@ -167,6 +167,33 @@ int attn_merge(const void* o_parts, const float* lse_parts, int n_parts, int B, 
                int D, void* o, float* lse, int dtype, void* stream);
 
 /*
+ * attn_bwd -- gradients of attn_fwd: dQ, dK, dV from dO.
+ *
+ * Page "Multi-Head Attention的计算本质与性能瓶颈" (mlqm.cn), §3.3 reserves a
+ * backward for every operator and states that masked connections carry no
+ * gradient; the formulas are the chain rule through the forward definition,
+ * with P recomputed from the forward's LSE (P = exp(scale q.k - LSE)):
+ *   dV = P^T dO,  dS = P * (dO V^T - D),  D = rowsum(dO * O),
+ *   dQ = scale dS K,  dK = scale dS^T Q.
+ * Dense layouts only (as attn_fwd without cu_seqlens):
+ *   q, o, dout, dq   [B, Sq, H, D]     k, v, dk, dv  [B, Sk, H, D]   (dtype)
+ *   lse              float [B, H, Sq]  the LSE attn_fwd returned for q, k, v
+ * causal as attn_fwd (top-left).  D 64 or 128.  All 16-bit pointers 16-byte
+ * aligned, lse 4-byte.  workspace: device scratch of at least
+ * attn_bwd_workspace(B, H, Sq, D) bytes, 256-byte aligned (an fp32 dQ
+ * accumulator and D); the call zeroes what it needs.  dQ is accumulated with
+ * fp32 atomics, so its last bits may differ between runs; dK and dV are
+ * deterministic.  Errors and ownership as attn_fwd; asynchronous on `stream`.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk,
+             int D, float scale, int causal, void* workspace, size_t workspace_bytes,
+             int dtype, void* stream);
+
+/* attn_bwd_workspace -- bytes of workspace attn_bwd needs (B*H*Sq*(D+1)*4, rounded). */
+int attn_bwd_workspace(int B, int H, int Sq, int D, size_t* bytes);
+
+/*
  * attn_check -- synchronise `stream`, then report and clear the device error
  * word of the current device: ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT,
  * ATTN_ERR_BAD_SEQLENS, or ATTN_ERR_CUDA if the stream itself failed.

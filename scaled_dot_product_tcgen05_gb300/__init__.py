@@ -14,12 +14,14 @@ from ._binding import (  # noqa: F401
     ATTN_OK,
     EXPORTED,
     AttnError,
+    attn_bwd,
     attn_check,
     attn_decode,
     attn_fwd,
     attn_fwd_raw,
     attn_fwd_window_raw,
     attn_merge,
+    bwd_workspace_bytes,
     decode_workspace_bytes,
     last_launch,
     load_library,

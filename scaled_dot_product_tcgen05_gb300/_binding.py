@@ -29,7 +29,8 @@ DTYPE_CODES = {torch.float16: 0, torch.bfloat16: 1}
 
 EXPORTED = ("attn_fwd", "attn_check", "attn_status_string", "attn_num_sms",
             "attn_last_launch", "attn_release", "attn_fwd_noalloc", "attn_fwd_window",
-            "attn_fwd_decode", "attn_decode_workspace", "attn_merge")
+            "attn_fwd_decode", "attn_decode_workspace", "attn_merge", "attn_bwd",
+            "attn_bwd_workspace")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -67,6 +68,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.attn_decode_workspace.restype = i
         lib.attn_merge.argtypes = [vp, vp, i, i, i, i, i, vp, vp, i, vp]
         lib.attn_merge.restype = i
+        lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp,
+                                 ctypes.c_size_t, i, vp]
+        lib.attn_bwd.restype = i
+        lib.attn_bwd_workspace.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_bwd_workspace.restype = i
         lib.attn_check.argtypes = [vp]
         lib.attn_check.restype = i
         lib.attn_status_string.argtypes = [i]
@@ -289,6 +295,58 @@ def attn_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, *,
     if st != ATTN_OK:
         raise AttnError(st, "attn_merge")
     return out, lse
+
+
+def bwd_workspace_bytes(B: int, H: int, Sq: int, D: int) -> int:
+    """Workspace bytes attn_bwd needs for these sizes."""
+    n = ctypes.c_size_t(0)
+    st = load_library().attn_bwd_workspace(B, H, Sq, D, ctypes.byref(n))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_workspace")
+    return int(n.value)
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+             dout: torch.Tensor, lse: torch.Tensor, *, causal: bool = False,
+             scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None,
+             dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
+             dv: Optional[torch.Tensor] = None, stream=None):
+    """Gradients (dQ, dK, dV) of :func:`attn_fwd` (dense layouts) from dO.
+
+    q, o, dout [B,Sq,H,D]; k, v [B,Sk,H,D]; lse fp32 [B,H,Sq] as returned by
+    attn_fwd for the same inputs.  ``workspace`` (uint8 CUDA tensor of at least
+    :func:`bwd_workspace_bytes`) is allocated when not given.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_16bit(name, t)
+    if not (q.dtype == k.dtype == v.dtype == o.dtype == dout.dtype):
+        raise ValueError("q, k, v, o, dout must share one dtype")
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("dense layouts only: q [B,Sq,H,D], k/v [B,Sk,H,D]")
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    if k.shape != (B, Sk, H, D) or v.shape != k.shape or o.shape != q.shape or \
+            dout.shape != q.shape:
+        raise ValueError("shape mismatch")
+    if lse.shape != (B, H, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, H, Sq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        need = bwd_workspace_bytes(B, H, Sq, D)
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        dq = torch.empty_like(q) if dq is None else dq
+        dk = torch.empty_like(k) if dk is None else dk
+        dv = torch.empty_like(v) if dv is None else dv
+        st = load_library().attn_bwd(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Sq, Sk, D,
+            ctypes.c_float(scale), 1 if causal else 0, workspace.data_ptr(), workspace.numel(),
+            DTYPE_CODES[q.dtype], _stream_handle(stream) or None)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_check(stream=None) -> int:

@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "attn.h"
+#include "bwd_kernel.cuh"
 #include "decode_kernel.cuh"
 #include "launch.cuh"
 #include "merge_kernel.cuh"
@@ -424,6 +425,123 @@ extern "C" int attn_merge(const void* o_parts, const float* lse_parts, int n_par
     cudaGetLastError();
     return ATTN_ERR_CUDA;
   }
+  return ATTN_OK;
+}
+
+// ---------------------------------------------------------------- backward
+namespace attn {
+namespace bwd {
+extern template cudaError_t launch_bwd<64, false>(const BwdParams&, const uint16_t*,
+                                                  const uint16_t*, float*, uint16_t*, int,
+                                                  cudaStream_t);
+extern template cudaError_t launch_bwd<64, true>(const BwdParams&, const uint16_t*,
+                                                 const uint16_t*, float*, uint16_t*, int,
+                                                 cudaStream_t);
+extern template cudaError_t launch_bwd<128, false>(const BwdParams&, const uint16_t*,
+                                                   const uint16_t*, float*, uint16_t*, int,
+                                                   cudaStream_t);
+extern template cudaError_t launch_bwd<128, true>(const BwdParams&, const uint16_t*,
+                                                  const uint16_t*, float*, uint16_t*, int,
+                                                  cudaStream_t);
+}  // namespace bwd
+namespace {
+long long bwd_ws_bytes(int B, int H, int Sq, int D) {
+  const long long acc = static_cast<long long>(B) * H * Sq * D * 4;
+  const long long dv = static_cast<long long>(B) * H * Sq * 4;
+  return ((acc + 255) / 256) * 256 + dv;
+}
+}  // namespace
+}  // namespace attn
+
+extern "C" int attn_bwd_workspace(int B, int H, int Sq, int D, size_t* bytes) {
+  if (!bytes) return ATTN_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (B < 0 || H < 1 || Sq < 0) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  *bytes = static_cast<size_t>(bwd_ws_bytes(B, H, Sq, D));
+  return ATTN_OK;
+}
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                        int H, int Sq, int Sk, int D, float scale, int causal, void* workspace,
+                        size_t workspace_bytes, int dtype, void* stream) {
+  // ---- argument checks (no CUDA call before these pass)
+  if (B < 0 || H < 1 || Sq < 0 || Sk < 1) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (dtype != ATTN_DTYPE_FP16 && dtype != ATTN_DTYPE_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || Sq == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(workspace, 256))
+    return ATTN_ERR_MISALIGNED;
+  const long long rows_q = static_cast<long long>(B) * Sq;
+  const long long rows_k = static_cast<long long>(B) * Sk;
+  if (rows_q > INT_MAX - 2 * bwd::kBN || rows_k > INT_MAX - 2 * bwd::kBM)
+    return ATTN_ERR_INVALID_ARG;
+  const long long units = static_cast<long long>(B) * H * ((Sk + bwd::kBM - 1) / bwd::kBM);
+  if (units > INT_MAX / 2) return ATTN_ERR_INVALID_ARG;
+  const long long need = bwd_ws_bytes(B, H, Sq, D);
+  if (static_cast<long long>(workspace_bytes) < need) return ATTN_ERR_INVALID_ARG;
+
+  // ---- device checks
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  DeviceState* ds = nullptr;
+  int st = device_state(dev, &ds);
+  if (st != ATTN_OK) return st;
+  const void* ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
+  for (const void* ptr : ptrs)
+    if (!on_device(ptr, dev)) return ATTN_ERR_INVALID_ARG;
+
+  // ---- parameters
+  bwd::BwdParams p;
+  const bool bf16 = dtype == ATTN_DTYPE_BF16;
+  if (encode_rows_heads_dim(&p.tm_q, q, rows_q, H, D, bf16) != ATTN_OK ||
+      encode_rows_heads_dim(&p.tm_do, dout, rows_q, H, D, bf16) != ATTN_OK ||
+      encode_rows_heads_dim(&p.tm_k, k, rows_k, H, D, bf16) != ATTN_OK ||
+      encode_rows_heads_dim(&p.tm_v, v, rows_k, H, D, bf16) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+  float* ws = static_cast<float*>(workspace);
+  p.lse = lse;
+  p.dq_acc = ws;
+  float* dvec = ws + ((static_cast<long long>(B) * H * Sq * D * 4 + 255) / 256) * 64;
+  p.dvec = dvec;
+  p.dk = dk;
+  p.dv = dv;
+  p.err = ds->err;
+  p.B = B;
+  p.H = H;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.timeout_ns = timeout_ns_from_env();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int grid = static_cast<int>(units < ds->sms ? units : ds->sms);
+  const uint16_t* o16 = static_cast<const uint16_t*>(o);
+  const uint16_t* do16 = static_cast<const uint16_t*>(dout);
+  uint16_t* dq16 = static_cast<uint16_t*>(dq);
+  cudaError_t e;
+  if (D == 64)
+    e = bf16 ? bwd::launch_bwd<64, true>(p, o16, do16, dvec, dq16, grid, s)
+             : bwd::launch_bwd<64, false>(p, o16, do16, dvec, dq16, grid, s);
+  else
+    e = bf16 ? bwd::launch_bwd<128, true>(p, o16, do16, dvec, dq16, grid, s)
+             : bwd::launch_bwd<128, false>(p, o16, do16, dvec, dq16, grid, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  t_last_grid = grid;
+  t_last_smem = D == 64 ? bwd::BLayout<64>::kAlloc : bwd::BLayout<128>::kAlloc;
   return ATTN_OK;
 }
 

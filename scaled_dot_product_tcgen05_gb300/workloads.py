@@ -46,6 +46,7 @@ class Workload:
     window: tuple = (-1, -1)        # (left, right) band of keys per query; -1 = unbounded
     global_q: int = 0               # leading query rows that ignore the window
     decode: bool = False            # Sq new queries against a full KV cache of Sk rows
+    backward: bool = False          # gradients dQ, dK, dV from a seeded dO
 
     @property
     def windowed(self) -> bool:
@@ -77,6 +78,7 @@ def standard_workloads() -> dict:
     6 window    B=1 H=32 S=131072 D=128 bf16 causal, sliding window of 4096 keys
                 (the query and the 4095 before it) with 64 global query rows: the
                 128K-context hybrid of page "长文本处理性能断层真相", §2.5
+    8 backward  B=1 H=32 S=16384 D=128 bf16 causal: dQ, dK, dV from a seeded dO
     7 decode    KV-cache decode (page "长文本处理性能断层真相", §2.2): one new token
                 per sequence against a 128K-token cache (B=1 H=32 D=128 bf16), and
                 a batch of 16 sequences with 32K-token caches and 4 new tokens each
@@ -96,6 +98,7 @@ def standard_workloads() -> dict:
     w["long128k_causal"] = _wl("long128k_causal", 5, 1, 32, 131072, 128, "bf16", True, draw=2)
     w["window128k_causal"] = _wl("window128k_causal", 6, 1, 32, 131072, 128, "bf16", True,
                                  window=(4095, 0), global_q=64)
+    w["bwd16k_causal"] = _wl("bwd16k_causal", 8, 1, 32, 16384, 128, "bf16", True, backward=True)
     w["decode128k_q1"] = Workload(name="decode128k_q1", wid=7, B=1, H=32, Sq=1, Sk=131072,
                                   D=128, dtype="bf16", causal=True, decode=True)
     w["decode32k_b16_q4"] = Workload(name="decode32k_b16_q4", wid=7, B=16, H=32, Sq=4,
@@ -159,7 +162,10 @@ def make_inputs(wl: Workload, heads: Optional[Sequence[int]] = None, pin: bool =
     q = make_tensor(wl.base_seed, 0, q_rows, wl.H, wl.D, wl.std[0], dt, heads, pin)
     k = make_tensor(wl.base_seed, 1, k_rows, wl.H, wl.D, wl.std[1], dt, heads, pin)
     v = make_tensor(wl.base_seed, 2, k_rows, wl.H, wl.D, wl.std[2], dt, heads, pin)
-    return dict(q=q, k=k, v=v, cu_seqlens_q=cu, cu_seqlens_k=cu, lengths=lengths)
+    out = dict(q=q, k=k, v=v, cu_seqlens_q=cu, cu_seqlens_k=cu, lengths=lengths)
+    if wl.backward:  # the output gradient dO, tensor index 3, N(0, 1)
+        out["do"] = make_tensor(wl.base_seed, 3, q_rows, wl.H, wl.D, 1.0, dt, heads, pin)
+    return out
 
 
 def sampled_heads_rows(wl: Workload, n_heads: int = 4, n_rows: int = 256):

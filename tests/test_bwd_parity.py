@@ -1,0 +1,128 @@
+"""GPU parity of the attention backward against the fp64 oracle.
+
+The backward (page "Multi-Head Attention的计算本质与性能瓶颈", §3.3: a reserved
+backward interface; masked connections carry no gradient) takes Q, K, V, O,
+dO and the forward's LSE.  Here O and LSE come from attn_fwd on the GPU, and
+the oracle's gradients from the exact fp64 definition.
+
+Tolerance (from the arithmetic), per gradient, relative to the RMS of the
+reference gradient:
+  * mean |err| <= 1e-2.  The kernel rounds P and dS to the input dtype
+    (relative u = 2^-9 for bf16, 2^-11 for fp16) before the products that
+    consume them and rounds dQ, dK, dV on output; every other step is fp32.  A
+    gradient entry sums many such terms with random signs, so its mean error is
+    about u of its RMS (0.002 for bf16): 5x margin.
+  * max |err| <= 0.15 (bf16), 0.06 (fp16).  D = rowsum(dO * O) uses the
+    16-bit O that the forward returned (the method's input), whose rounding
+    gives D an error up to u * |dO| |O| (about 0.25 for unit-variance rows at
+    D = 128, bf16).  In rows whose softmax is nearly one-hot, dP - D nearly
+    cancels, so that error reaches dS unattenuated and dQ_i carries up to
+    scale * dD * max|K| (about 0.09 absolute here, 0.05-0.09 of the RMS
+    observed on the causal cases): the bound is 1.6-2.5x that worst case, 4x
+    smaller for fp16.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import scaled_dot_product_tcgen05_gb300 as pkg
+from oracle.sdpa_oracle import attention_backward_dense
+
+pytestmark = pytest.mark.gpu
+
+BF, FP = torch.bfloat16, torch.float16
+DEV = "cuda:0"
+MEAN_REL = 1e-2
+MAX_REL = {torch.bfloat16: 0.15, torch.float16: 0.06}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkg.load_library()
+
+
+def _case(seed, B, H, Sq, Sk, D, dt):
+    g = torch.Generator().manual_seed(seed)
+    mk = lambda S: torch.randn(B, S, H, D, generator=g).to(dt)  # noqa: E731
+    return mk(Sq), mk(Sk), mk(Sk), mk(Sq)
+
+
+def compare_grads(got, ref, what):
+    stats = {}
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        gg = g.float().cpu().numpy().astype(np.float64)
+        sel = ~np.isnan(r)
+        assert np.all(np.isfinite(gg[sel])), f"{what}: non-finite {name}"
+        rms = max(float(np.sqrt(np.mean(r[sel] ** 2))), 1e-30)
+        d = np.abs(gg[sel] - r[sel])
+        stats[name] = (float(d.mean() / rms), float(d.max() / rms))
+        bound = MAX_REL[g.dtype]
+        assert stats[name][0] <= MEAN_REL and stats[name][1] <= bound, f"{what}: {name} {stats}"
+    return stats
+
+
+def _run(q, k, v, do, causal, scale):
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = pkg.attn_fwd(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = pkg.attn_bwd(qd, kd, vd, o, dod, lse, causal=causal, scale=scale)
+    st = pkg.attn_check()
+    assert st == pkg.ATTN_OK, pkg.status_string(st)
+    return dq, dk, dv
+
+
+CASES = [
+    # (B, H, Sq, Sk, D, dtype, causal)
+    (1, 2, 256, 256, 128, BF, True),
+    (1, 2, 256, 256, 128, BF, False),
+    (2, 2, 300, 300, 64, FP, True),
+    (1, 3, 128, 384, 128, BF, False),
+    (1, 2, 400, 200, 64, BF, False),
+    (2, 1, 129, 129, 128, FP, False),
+    (1, 2, 200, 300, 128, BF, True),     # keys 200.. seen by no query: zero dK, dV
+    (1, 2, 300, 200, 64, FP, True),
+    (1, 1, 1, 1, 64, BF, True),
+    (1, 4, 1024, 1024, 128, BF, True),
+    (2, 2, 777, 777, 64, BF, True),
+]
+
+
+def _id(c):
+    return "B{}H{}q{}k{}D{}{}{}".format(c[0], c[1], c[2], c[3], c[4],
+                                        "bf" if c[5] == BF else "fp", "c" if c[6] else "")
+
+
+@pytest.mark.parametrize("case", CASES, ids=_id)
+def test_bwd_parity(case):
+    B, H, Sq, Sk, D, dt, causal = case
+    q, k, v, do = _case(Sq * 5 + Sk + D, B, H, Sq, Sk, D, dt)
+    scale = 1.0 / math.sqrt(D)
+    got = _run(q, k, v, do, causal, scale)
+    ref = attention_backward_dense(q, k, v, do, scale, causal)
+    compare_grads(got, ref, _id(case))
+    if causal and Sk > Sq:  # keys no query sees get exactly zero gradient
+        assert torch.all(got[1][:, Sq:] == 0) and torch.all(got[2][:, Sq:] == 0)
+
+
+def test_bwd_peaked_scores():
+    """Q, K ~ N(0, 16): a peaked softmax stresses P = exp(S - LSE) recomputation."""
+    g = torch.Generator().manual_seed(77)
+    B, H, S, D = 1, 2, 512, 128
+    q = (torch.randn(B, S, H, D, generator=g) * 4).to(BF)
+    k = (torch.randn(B, S, H, D, generator=g) * 4).to(BF)
+    v = torch.randn(B, S, H, D, generator=g).to(BF)
+    do = torch.randn(B, S, H, D, generator=g).to(BF)
+    got = _run(q, k, v, do, True, 1 / math.sqrt(D))
+    ref = attention_backward_dense(q, k, v, do, 1 / math.sqrt(D), True)
+    compare_grads(got, ref, "peaked")
+
+
+def test_bwd_dk_dv_deterministic():
+    q, k, v, do = _case(3, 1, 2, 600, 600, 128, BF)
+    a = _run(q, k, v, do, True, 0.09)
+    b = _run(q, k, v, do, True, 0.09)
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    assert torch.allclose(a[0].float(), b[0].float(), atol=1e-2, rtol=0)

@@ -20,7 +20,8 @@ pytestmark = pytest.mark.gpu
 
 WL = W.standard_workloads()
 # workloads the oracle checks in full (the long-context ones are sampled below)
-SMALL = [n for n, w in WL.items() if w.Sq <= 4096 and not w.windowed and not w.decode]
+SMALL = [n for n, w in WL.items()
+         if w.Sq <= 4096 and not w.windowed and not w.decode and not w.backward]
 
 
 @pytest.fixture(scope="module", autouse=True)
