@@ -14,7 +14,8 @@
 // head, 128-key tile).  Keys are the M dimension of every product the unit
 // accumulates, so dK and dV stay in tensor memory for the whole unit:
 //   TMEM columns: S^T | dP^T | dV | dK (128, 128, D, D); dQ of a step is
-//   written over S^T once P^T has been consumed.
+//   written over dP^T once dS^T has been consumed, so S^T of the next query
+//   tile can be computed while this step's dS is still being formed.
 //   * warp 9 (one lane): TMA for the unit's K and V tiles and, per step
 //     (128 queries), Q and dO tiles into a 2-stage ring;
 //   * warp 8 (one lane): tcgen05.mma
@@ -100,6 +101,12 @@ __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+
+// dst[0..3] += v (fp32, relaxed, no return value: the warp does not wait)
+__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+               ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
 template <bool BF16>
@@ -317,21 +324,19 @@ __device__ void dq_role(const BwdParams& p, uint32_t tmem, uint32_t bars, const 
       ptx::tc_fence_after();
       uint32_t v[D];
       if constexpr (D == 128) {
-        ptx::tmem_ld_x128(tmem + lane_bits + L::kColS, v);
+        ptx::tmem_ld_x128(tmem + lane_bits + L::kColDP, v);
       } else {
-        ptx::tmem_ld_x64(tmem + lane_bits + L::kColS, v);
+        ptx::tmem_ld_x64(tmem + lane_bits + L::kColDP, v);
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(L::DQE));
       const int q = (w.i0 + j) * kBN + r;
       if (q < p.Sq) {
-        float4* dst = reinterpret_cast<float4*>(
-            p.dq_acc + ((static_cast<long long>(w.b) * p.H + w.h) * p.Sq + q) * D);
+        float* dst = p.dq_acc + ((static_cast<long long>(w.b) * p.H + w.h) * p.Sq + q) * D;
 #pragma unroll
         for (int c = 0; c < D / 4; ++c)
-          atomicAdd(dst + c, make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                                         __uint_as_float(v[4 * c + 2]),
-                                         __uint_as_float(v[4 * c + 3])));
+          red_add_v4(dst + 4 * c, __uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                     __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
       }
     }
     // ---- dK (times scale) and dV of this key tile
@@ -380,27 +385,39 @@ __device__ void mma_loop(const BwdParams& p, uint32_t smem, uint32_t tmem, uint3
   const uint32_t tS = tmem + L::kColS, tDP = tmem + L::kColDP;
   const uint32_t tDV = tmem + L::kColDV, tDK = tmem + L::kColDK;
   uint32_t g = 0, kv_cnt = 0, u_cnt = 0;
+  // S^T(g) = K Q_g^T into the S^T columns (Q_g of ring stage g % 2)
+  auto issue_s = [&](uint32_t gg) -> bool {
+    const uint32_t st = gg & 1u;
+    if (!wait_bar(bar(L::QF0 + st), (gg >> 1) & 1u, ctl)) return false;
+    ptx::tc_fence_after();
+    const uint64_t dQ_kmaj = ptx::desc_sw128(smem + L::kQOff + st * L::kTile, 16, 1024);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint32_t off = ((ks >> 2) * L::kBlk + (ks & 3) * 32) >> 4;
+      ptx::mma_ss(tS, dK_kmaj + off, dQ_kmaj + off, kIdS, ks > 0 ? 1u : 0u);
+    }
+    ptx::mma_commit(bar(L::SF));
+    return true;
+  };
+  // Order per step g (one issuing thread, so tensor memory reuse follows
+  // issue order): S^T(g) [issued during step g-1 when in the same unit],
+  // dP^T(g) once dQ(g-1) has been read out of the dP^T columns, dV(g) once P(g)
+  // is in TMEM, S^T(g+1) (P(g) is consumed by dV(g) before it), then dK(g) and
+  // dQ(g) = dS K into the dP^T columns once dS(g) is ready.
   BUnit w;
   for (int k = 0; bwd_unit(p, k, w); ++k) {
     if (w.n == 0) continue;
     if (!wait_bar(bar(L::KVF), kv_cnt & 1u, ctl)) return;
     ++kv_cnt;
     ptx::tc_fence_after();
+    if (!issue_s(g)) return;
     for (int j = 0; j < w.n; ++j, ++g) {
       const uint32_t st = g & 1u;
       const uint32_t qbase = smem + L::kQOff + st * L::kTile;
       const uint32_t dobase = smem + L::kDoOff + st * L::kDoStage;
-      if (!wait_bar(bar(L::QF0 + st), (g >> 1) & 1u, ctl)) return;
-      if (g > 0 && !wait_bar(bar(L::DQE), (g - 1) & 1u, ctl)) return;  // S^T columns free
+      if (g > 0 && !wait_bar(bar(L::DQE), (g - 1) & 1u, ctl)) return;  // dP^T columns free
       ptx::tc_fence_after();
-      const uint64_t dQ_kmaj = ptx::desc_sw128(qbase, 16, 1024);
       const uint64_t dDo_kmaj = ptx::desc_sw128(dobase, 16, 1024);
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {  // S^T = K Q^T
-        const uint32_t off = ((ks >> 2) * L::kBlk + (ks & 3) * 32) >> 4;
-        ptx::mma_ss(tS, dK_kmaj + off, dQ_kmaj + off, kIdS, ks > 0 ? 1u : 0u);
-      }
-      ptx::mma_commit(bar(L::SF));
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {  // dP^T = V dO^T
         const uint32_t off = ((ks >> 2) * L::kBlk + (ks & 3) * 32) >> 4;
@@ -416,6 +433,7 @@ __device__ void mma_loop(const BwdParams& p, uint32_t smem, uint32_t tmem, uint3
         ptx::mma_ts(tDV, tS + ks * 8, dDo_mn + ((ks * 2048) >> 4), kIdAcc,
                     (j > 0 || ks > 0) ? 1u : 0u);
       ptx::mma_commit(bar(L::DVD));
+      if (j + 1 < w.n && !issue_s(g + 1)) return;  // next query tile of this unit
       if (!wait_bar(bar(L::DSR), g & 1u, ctl)) return;
       ptx::tc_fence_after();
       const uint64_t dQ_mn = ptx::desc_sw128(qbase, L::kBlk, 1024);
@@ -426,7 +444,7 @@ __device__ void mma_loop(const BwdParams& p, uint32_t smem, uint32_t tmem, uint3
                     (j > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
       for (int ks = 0; ks < kBM / 16; ++ks)  // dQ = dS K (over this tile's keys)
-        ptx::mma_ss(tS, dDs_mn + ((ks * 2048) >> 4), dK_mn + ((ks * 2048) >> 4), kIdDq,
+        ptx::mma_ss(tDP, dDs_mn + ((ks * 2048) >> 4), dK_mn + ((ks * 2048) >> 4), kIdDq,
                     ks > 0 ? 1u : 0u);
       ptx::mma_commit(bar(L::DQF));
       ptx::mma_commit(bar(L::QE0 + st));
