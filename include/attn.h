@@ -178,7 +178,9 @@ int attn_merge(const void* o_parts, const float* lse_parts, int n_parts, int B, 
  * Dense layouts only (as attn_fwd without cu_seqlens):
  *   q, o, dout, dq   [B, Sq, H, D]     k, v, dk, dv  [B, Sk, H, D]   (dtype)
  *   lse              float [B, H, Sq]  the LSE attn_fwd returned for q, k, v
- * causal as attn_fwd (top-left).  D 64 or 128.  All 16-bit pointers 16-byte
+ * causal as attn_fwd (top-left).  D 64 or 128.  scale must be finite and
+ * non-zero (ATTN_ERR_UNSUPPORTED for 0: the LSE term is carried as -LSE/scale).
+ * All 16-bit pointers 16-byte
  * aligned, lse 4-byte.  workspace: device scratch of at least
  * attn_bwd_workspace(B, H, Sq, D) bytes, 256-byte aligned (an fp32 dQ
  * accumulator and D); the call zeroes what it needs.  dQ is accumulated with
@@ -190,7 +192,11 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              int D, float scale, int causal, void* workspace, size_t workspace_bytes,
              int dtype, void* stream);
 
-/* attn_bwd_workspace -- bytes of workspace attn_bwd needs (B*H*Sq*(D+1)*4, rounded). */
+/*
+ * attn_bwd_workspace -- bytes of workspace attn_bwd needs: an fp32 dQ
+ * accumulator (B*H*Sq*D*4, rounded up to 256) and 8 KiB per 128-query tile
+ * per (sequence, head) for the per-query terms -LSE/scale and -D.
+ */
 int attn_bwd_workspace(int B, int H, int Sq, int D, size_t* bytes);
 
 /*

@@ -431,24 +431,20 @@ extern "C" int attn_merge(const void* o_parts, const float* lse_parts, int n_par
 // ---------------------------------------------------------------- backward
 namespace attn {
 namespace bwd {
-extern template cudaError_t launch_bwd<64, false>(const BwdParams&, const uint16_t*,
-                                                  const uint16_t*, float*, uint16_t*, int,
-                                                  cudaStream_t);
-extern template cudaError_t launch_bwd<64, true>(const BwdParams&, const uint16_t*,
-                                                 const uint16_t*, float*, uint16_t*, int,
-                                                 cudaStream_t);
-extern template cudaError_t launch_bwd<128, false>(const BwdParams&, const uint16_t*,
-                                                   const uint16_t*, float*, uint16_t*, int,
-                                                   cudaStream_t);
-extern template cudaError_t launch_bwd<128, true>(const BwdParams&, const uint16_t*,
-                                                  const uint16_t*, float*, uint16_t*, int,
-                                                  cudaStream_t);
+extern template cudaError_t launch_bwd<64, false>(const BwdParams&, const uint16_t*, const uint16_t*, const float*, uint8_t*, uint16_t*, int, cudaStream_t);
+extern template cudaError_t launch_bwd<64, true>(const BwdParams&, const uint16_t*, const uint16_t*, const float*, uint8_t*, uint16_t*, int, cudaStream_t);
+extern template cudaError_t launch_bwd<128, false>(const BwdParams&, const uint16_t*, const uint16_t*, const float*, uint8_t*, uint16_t*, int, cudaStream_t);
+extern template cudaError_t launch_bwd<128, true>(const BwdParams&, const uint16_t*, const uint16_t*, const float*, uint8_t*, uint16_t*, int, cudaStream_t);
 }  // namespace bwd
 namespace {
+// fp32 dQ accumulator, then the bias tiles of the two products (-LSE/scale
+// and -D, 2 x 4 KiB per 128-query tile).
+long long bwd_acc_bytes(int B, int H, int Sq, int D) {
+  return ((static_cast<long long>(B) * H * Sq * D * 4 + 255) / 256) * 256;
+}
 long long bwd_ws_bytes(int B, int H, int Sq, int D) {
-  const long long acc = static_cast<long long>(B) * H * Sq * D * 4;
-  const long long dv = static_cast<long long>(B) * H * Sq * 4;
-  return ((acc + 255) / 256) * 256 + dv;
+  const long long tiles = static_cast<long long>(B) * H * ((Sq + bwd::kBN - 1) / bwd::kBN);
+  return bwd_acc_bytes(B, H, Sq, D) + tiles * 2 * bwd::kBiasBytes;
 }
 }  // namespace
 }  // namespace attn
@@ -471,6 +467,7 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (dtype != ATTN_DTYPE_FP16 && dtype != ATTN_DTYPE_BF16) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (scale == 0.0f) return ATTN_ERR_UNSUPPORTED;  // the LSE term is carried as -LSE/scale
   if (B == 0 || Sq == 0) return ATTN_OK;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
     return ATTN_ERR_INVALID_ARG;
@@ -508,11 +505,9 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
       encode_rows_heads_dim(&p.tm_k, k, rows_k, H, D, bf16) != ATTN_OK ||
       encode_rows_heads_dim(&p.tm_v, v, rows_k, H, D, bf16) != ATTN_OK)
     return ATTN_ERR_CUDA;
-  float* ws = static_cast<float*>(workspace);
-  p.lse = lse;
-  p.dq_acc = ws;
-  float* dvec = ws + ((static_cast<long long>(B) * H * Sq * D * 4 + 255) / 256) * 64;
-  p.dvec = dvec;
+  p.dq_acc = static_cast<float*>(workspace);
+  uint8_t* bias = static_cast<uint8_t*>(workspace) + bwd_acc_bytes(B, H, Sq, D);
+  p.bias = bias;
   p.dk = dk;
   p.dv = dv;
   p.err = ds->err;
@@ -531,11 +526,11 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   uint16_t* dq16 = static_cast<uint16_t*>(dq);
   cudaError_t e;
   if (D == 64)
-    e = bf16 ? bwd::launch_bwd<64, true>(p, o16, do16, dvec, dq16, grid, s)
-             : bwd::launch_bwd<64, false>(p, o16, do16, dvec, dq16, grid, s);
+    e = bf16 ? bwd::launch_bwd<64, true>(p, o16, do16, lse, bias, dq16, grid, s)
+             : bwd::launch_bwd<64, false>(p, o16, do16, lse, bias, dq16, grid, s);
   else
-    e = bf16 ? bwd::launch_bwd<128, true>(p, o16, do16, dvec, dq16, grid, s)
-             : bwd::launch_bwd<128, false>(p, o16, do16, dvec, dq16, grid, s);
+    e = bf16 ? bwd::launch_bwd<128, true>(p, o16, do16, lse, bias, dq16, grid, s)
+             : bwd::launch_bwd<128, false>(p, o16, do16, lse, bias, dq16, grid, s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_CUDA;

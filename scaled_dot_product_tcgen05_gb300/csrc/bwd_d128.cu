@@ -5,8 +5,10 @@
 namespace attn {
 namespace bwd {
 template cudaError_t launch_bwd<128, false>(const BwdParams&, const uint16_t*, const uint16_t*,
-                                           float*, uint16_t*, int, cudaStream_t);
+                                           const float*, uint8_t*, uint16_t*, int,
+                                           cudaStream_t);
 template cudaError_t launch_bwd<128, true>(const BwdParams&, const uint16_t*, const uint16_t*,
-                                          float*, uint16_t*, int, cudaStream_t);
+                                          const float*, uint8_t*, uint16_t*, int,
+                                          cudaStream_t);
 }  // namespace bwd
 }  // namespace attn

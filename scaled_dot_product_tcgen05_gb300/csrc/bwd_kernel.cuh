@@ -24,16 +24,22 @@
 //       dV  += P^T dO     (TS: P^T from TMEM, dO MN-major)
 //       dK  += dS^T Q     (TS: dS^T from TMEM, Q MN-major)
 //       dQ   = dS K       (SS: dS MN-major from shared memory, K MN-major)
-//   * warps 0-3: one thread per key (TMEM lane): P^T = 2^(S^T scale log2e -
-//     LSE log2e) written back as 16-bit over S^T, then dS^T = P^T (dP^T - D)
-//     written as 16-bit over dP^T and into the dO stage (whose dO the dV and
-//     dP^T products have finished reading), as the A operand of dQ;
+//   * the per-query terms -LSE/scale and -D enter the products themselves: one
+//     extra K = 16 step multiplies a ones column (in shared memory) by a
+//     three-part bf16 split of each term (per query tile, written by the
+//     pre-pass), so S^T arrives as S^T - LSE/scale and dP^T as dP^T - D and
+//     the per-element loops below need no per-column loads;
+//   * warps 0-3: one thread per key (TMEM lane): P^T = 2^(scale log2e S'^T)
+//     written back as 16-bit over S^T, then dS^T = P^T dP'^T written as 16-bit
+//     over dP^T and into the dO stage (whose dO the dV and dP^T products have
+//     finished reading), as the A operand of dQ;
 //   * warps 4-7: one thread per query row: dQ of each step is added with
 //     fp32 atomics to a [B, H, Sq, D] accumulator; at the end of the unit they
 //     write dK (times scale) and dV.
 // Every wait is bounded (same error word and abort flag as the forward).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "fwd_kernel.cuh"
@@ -48,11 +54,14 @@ constexpr int kDqWarp0 = 4;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kTmemCols = 512;
+// A 128 x 16 16-bit operand without swizzle: 8 x 8 core matrices of 8 rows x
+// 16 B; row r, element k at (r / 8) * 256 + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2.
+constexpr int kBiasBytes = 4096;
+constexpr int kBiasParts = 3;  // a term is the sum of three bf16 values
 
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // [B*S, H, D] 16-bit, box 64 x 1 x 128, 128-B swizzle
-  const float* lse;                      // [B, H, Sq] natural log
-  const float* dvec;                     // [B, H, Sq]: sum_d dO * O
+  const uint8_t* bias;                   // [B*H][query tile][2][kBiasBytes]: -LSE/scale, -D
   float* dq_acc;                         // [B, H, Sq, D] fp32, zero on entry
   void* dk;                              // [B, Sk, H, D]
   void* dv;
@@ -71,11 +80,11 @@ struct BLayout {
   static constexpr int kVOff = kTile;
   static constexpr int kQOff = 2 * kTile;              // 2 stages
   static constexpr int kDoOff = kQOff + 2 * kTile;     // 2 stages of kDoStage
-  static constexpr int kStatOff = kDoOff + 2 * kDoStage;  // [2][2][128]: -LSE*log2e, D
-  static constexpr int kBarOff = kStatOff + 2 * 2 * kBN * 4;
+  static constexpr int kOnesOff = kDoOff + 2 * kDoStage;  // 128 x 16 ones column (bf16)
+  static constexpr int kBiasOff = kOnesOff + kBiasBytes;   // 2 stages x (S bias, D bias)
+  static constexpr int kBarOff = kBiasOff + 2 * 2 * kBiasBytes;
   enum : int {
-    KVF = 0, KVE, QF0, QF1, QE0, QE1, SF, DPF, PR, DVD, DSR, DQF, DQE, OF, AE, ST0, ST1, DONE,
-    kNumBars
+    KVF = 0, KVE, QF0, QF1, QE0, QE1, SF, DPF, PR, DVD, DSR, DQF, DQE, OF, AE, DONE, kNumBars
   };
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag
   static constexpr int kBytes = kMiscOff + 16;
@@ -86,6 +95,31 @@ struct BLayout {
 // ---------------------------------------------------------------- helpers
 __host__ __device__ constexpr uint32_t idesc_ab(bool bf16, int M, int N, bool a_mn, bool b_mn) {
   return ptx::idesc_f16_f32acc(bf16, M, N, b_mn) | ((a_mn ? 1u : 0u) << 15);
+}
+
+// Descriptor of a K-major operand without swizzle (layout above): leading
+// byte offset 128 (next core matrix along K), stride byte offset 256 (next 8
+// rows), version bit 46, swizzle mode 0.
+__device__ __forceinline__ uint64_t desc_noswz(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128 >> 4) << 16;
+  d |= static_cast<uint64_t>(256 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar) : "memory");
+}
+
+__host__ __device__ constexpr int bias_offset(int r, int k) {
+  return (r / 8) * 256 + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2;
 }
 
 // generic-proxy shared-memory writes -> later tensor-core (async proxy) reads
@@ -165,8 +199,8 @@ struct StepIter {
 
 // ------------------------------------------------------------- P and dS
 template <int D, bool BF16>
-__device__ void ds_role(const BwdParams& p, uint32_t tmem, uint32_t smem, uint8_t* base,
-                        uint32_t bars, const Ctl& ctl) {
+__device__ void ds_role(const BwdParams& p, uint32_t tmem, uint8_t* base, uint32_t bars,
+                        const Ctl& ctl) {
   using L = BLayout<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -175,38 +209,13 @@ __device__ void ds_role(const BwdParams& p, uint32_t tmem, uint32_t smem, uint8_
   const uint32_t tS = tmem + lane_bits + L::kColS;
   const uint32_t tDP = tmem + lane_bits + L::kColDP;
   auto bar = [&](int i) { return bars + 8u * i; };
-  float* const stats = reinterpret_cast<float*>(base + L::kStatOff);
-  const float log2e = 1.4426950408889634f;
+  const uint64_t c2 = ptx::f2(p.scale_log2, p.scale_log2);
 
   StepIter cur;
   cur.start(p);
-  // statistics of the first step (each thread: column r of the query tile)
-  float nl_next = 0.0f, dv_next = 0.0f;
-  auto fetch = [&](const StepIter& it) {
-    const int q = (it.w.i0 + it.j) * kBN + r;
-    nl_next = 0.0f;
-    dv_next = 0.0f;
-    if (q < p.Sq) {
-      const long long idx = (static_cast<long long>(it.w.b) * p.H + it.w.h) * p.Sq + q;
-      const float l = __ldg(p.lse + idx);
-      nl_next = l == -INFINITY ? -INFINITY : -l * log2e;
-      dv_next = __ldg(p.dvec + idx);
-    }
-  };
-  if (cur.ok) fetch(cur);
   for (uint32_t g = 0; cur.ok; ++g) {
     const BUnit w = cur.w;
     const int i = w.i0 + cur.j;
-    // ---- publish this step's statistics, prefetch the next step's
-    float* const st = stats + (g & 1u) * 2 * kBN;
-    st[r] = nl_next;
-    st[kBN + r] = dv_next;
-    StepIter nxt = cur;
-    nxt.next(p);
-    if (nxt.ok) fetch(nxt);
-    ptx::mbar_arrive(bar(L::ST0 + (g & 1u)));
-    if (!wait_bar_warp(bar(L::ST0 + (g & 1u)), (g >> 1) & 1u, ctl)) return;
-
     const int key = w.kt * kBM + r;
     const int qb = i * kBN;
     // columns c (query qb + c) visible to this key: c >= cmin and qb + c < Sq
@@ -215,7 +224,7 @@ __device__ void ds_role(const BwdParams& p, uint32_t tmem, uint32_t smem, uint8_
     const bool row_ok = key < p.Sk;
     const bool full = row_ok && cmin <= 0 && cmax >= kBN - 1;
 
-    // ---- P^T = 2^(S^T * scale * log2e - LSE * log2e), 16-bit, over S^T
+    // ---- P^T = 2^(scale log2e (S^T - LSE / scale)), 16-bit, over S^T
     if (!wait_bar_warp(bar(L::SF), g & 1u, ctl)) return;
     ptx::tc_fence_after();
     uint32_t pk[64];
@@ -223,13 +232,10 @@ __device__ void ds_role(const BwdParams& p, uint32_t tmem, uint32_t smem, uint8_
     for (int c0 = 0; c0 < kBN; c0 += 32) {
       uint32_t s[32];
       ptx::tmem_ld_x32(tS + c0, s);
-      const float2* nl = reinterpret_cast<const float2*>(st + c0);
 #pragma unroll
       for (int c = 0; c < 32; c += 2) {
-        const float2 n2 = nl[c / 2];
         float x0, x1;
-        ptx::f2_split(ptx::f2_fma(ptx::f2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])),
-                                  ptx::f2(p.scale_log2, p.scale_log2), ptx::f2(n2.x, n2.y)),
+        ptx::f2_split(ptx::f2_mul(ptx::f2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), c2),
                       x0, x1);
         float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
         if (!full) {
@@ -257,18 +263,14 @@ __device__ void ds_role(const BwdParams& p, uint32_t tmem, uint32_t smem, uint8_
     for (int c0 = 0; c0 < kBN; c0 += 32) {
       uint32_t dp[32];
       ptx::tmem_ld_x32(tDP + c0, dp);
-      const float2* dd = reinterpret_cast<const float2*>(st + kBN + c0);
       uint32_t dk[16];
 #pragma unroll
       for (int c = 0; c < 32; c += 2) {
         float p0, p1;
         unpack2<BF16>(pk[(c0 + c) / 2], p0, p1);
-        const float2 d2 = dd[c / 2];
         float a, b;
-        ptx::f2_split(ptx::f2_mul(ptx::f2(p0, p1),
-                                  ptx::f2_add(ptx::f2(__uint_as_float(dp[c]),
-                                                      __uint_as_float(dp[c + 1])),
-                                              ptx::f2(-d2.x, -d2.y))),
+        ptx::f2_split(ptx::f2_mul(ptx::f2(p0, p1), ptx::f2(__uint_as_float(dp[c]),
+                                                            __uint_as_float(dp[c + 1]))),
                       a, b);
         dk[c / 2] = ptx::pack2<BF16>(a, b);
       }
@@ -287,9 +289,8 @@ __device__ void ds_role(const BwdParams& p, uint32_t tmem, uint32_t smem, uint8_
     fence_proxy_async_smem();
     ptx::tc_fence_before();
     ptx::mbar_arrive(bar(L::DSR));
-    cur = nxt;
+    cur.next(p);
   }
-  (void)smem;
 }
 
 // -------------------------------------------------- dQ and the dK/dV epilogue
@@ -378,6 +379,8 @@ __device__ void mma_loop(const BwdParams& p, uint32_t smem, uint32_t tmem, uint3
   constexpr uint32_t kIdS = idesc_ab(BF16, kBM, kBN, false, false);   // S^T, dP^T
   constexpr uint32_t kIdAcc = idesc_ab(BF16, kBM, D, false, true);    // dV, dK (A from TMEM)
   constexpr uint32_t kIdDq = idesc_ab(BF16, kBN, D, true, true);      // dQ
+  constexpr uint32_t kIdBias = idesc_ab(true, kBM, kBN, false, false); // bf16 ones x bias
+  const uint64_t dOnes = desc_noswz(smem + L::kOnesOff);
   auto bar = [&](int i) { return bars + 8u * i; };
   const uint64_t dK_kmaj = ptx::desc_sw128(smem + L::kKOff, 16, 1024);
   const uint64_t dV_kmaj = ptx::desc_sw128(smem + L::kVOff, 16, 1024);
@@ -396,6 +399,8 @@ __device__ void mma_loop(const BwdParams& p, uint32_t smem, uint32_t tmem, uint3
       const uint32_t off = ((ks >> 2) * L::kBlk + (ks & 3) * 32) >> 4;
       ptx::mma_ss(tS, dK_kmaj + off, dQ_kmaj + off, kIdS, ks > 0 ? 1u : 0u);
     }
+    // + ones x (-LSE / scale): S'^T = S^T - LSE / scale per query column
+    ptx::mma_ss(tS, dOnes, desc_noswz(smem + L::kBiasOff + st * 2 * kBiasBytes), kIdBias, 1u);
     ptx::mma_commit(bar(L::SF));
     return true;
   };
@@ -423,6 +428,9 @@ __device__ void mma_loop(const BwdParams& p, uint32_t smem, uint32_t tmem, uint3
         const uint32_t off = ((ks >> 2) * L::kBlk + (ks & 3) * 32) >> 4;
         ptx::mma_ss(tDP, dV_kmaj + off, dDo_kmaj + off, kIdS, ks > 0 ? 1u : 0u);
       }
+      // + ones x (-D): dP'^T = dP^T - D per query column
+      ptx::mma_ss(tDP, dOnes, desc_noswz(smem + L::kBiasOff + (st * 2 + 1) * kBiasBytes),
+                  kIdBias, 1u);
       ptx::mma_commit(bar(L::DPF));
       if (!wait_bar(bar(L::PR), g & 1u, ctl)) return;
       if (j == 0 && u_cnt > 0 && !wait_bar(bar(L::AE), (u_cnt - 1) & 1u, ctl)) return;
@@ -478,8 +486,12 @@ __device__ void load_loop(const BwdParams& p, uint32_t smem, uint32_t bars, cons
     for (int j = 0; j < w.n; ++j, ++g) {
       const uint32_t st = g & 1u;
       if (g >= 2 && !wait_bar(bar(L::QE0 + st), ((g >> 1) - 1) & 1u, ctl)) return;
-      ptx::mbar_arrive_expect_tx(bar(L::QF0 + st), 2 * L::kTile);
+      ptx::mbar_arrive_expect_tx(bar(L::QF0 + st), 2 * L::kTile + 2 * kBiasBytes);
       const int qrow = w.b * p.Sq + (w.i0 + j) * kBN;
+      const int nq = (p.Sq + kBN - 1) / kBN;
+      const long long tile = (static_cast<long long>(w.b) * p.H + w.h) * nq + w.i0 + j;
+      bulk_load(smem + L::kBiasOff + st * 2 * kBiasBytes, p.bias + tile * 2 * kBiasBytes,
+                2 * kBiasBytes, bar(L::QF0 + st));
 #pragma unroll
       for (int blk = 0; blk < D / 64; ++blk) {
         ptx::tma_load_3d(smem + L::kQOff + st * L::kTile + blk * L::kBlk, &p.tm_q,
@@ -506,12 +518,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
-      const bool many = i == L::PR || i == L::DSR || i == L::DQE || i == L::AE ||
-                        i == L::ST0 || i == L::ST1;
+      const bool many = i == L::PR || i == L::DSR || i == L::DQE || i == L::AE;
       ptx::mbar_init(bars + 8u * i, many ? 128u : 1u);
     }
     *abort_flag = 0;
     ptx::fence_mbar_init();
+  }
+  if (threadIdx.x < kBM) {  // the ones column of the bias products: k = 0, 1, 2 are 1.0 (bf16)
+    uint8_t* const ones = base + L::kOnesOff;
+    const int r = threadIdx.x;
+    *reinterpret_cast<uint4*>(ones + bias_offset(r, 0)) =
+        make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u);
+    *reinterpret_cast<uint4*>(ones + bias_offset(r, 8)) = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
   }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -530,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   const Ctl ctl{abort_flag, p.err, p.timeout_ns};
 
   if (warp < kDqWarp0) {
-    ds_role<D, BF16>(p, tmem, smem, base, bars, ctl);
+    ds_role<D, BF16>(p, tmem, base, bars, ctl);
   } else if (warp < kMmaWarp) {
     dq_role<D, BF16>(p, tmem, bars, ctl);
   } else if (warp == kMmaWarp) {
@@ -558,33 +577,65 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 }
 
 // ------------------------------------------------ pre- and post-processing
-// D[b, h, q] = sum_d dO[b, q, h, d] * O[b, q, h, d] (fp32), one warp per row.
+// v = hi + mid + lo in bf16 (the residual of three parts is about 2^-27 |v|).
+__device__ __forceinline__ void split3_bf16(float v, uint16_t (&out)[kBiasParts]) {
+  float rest = v;
+#pragma unroll
+  for (int i = 0; i < kBiasParts; ++i) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(rest);
+    out[i] = __bfloat16_as_ushort(b);
+    rest -= __bfloat162float(b);
+  }
+}
+
+// Per query row (b, h, q) of every query tile, q < Sq padded to whole tiles:
+// the bias operands of the two products, -LSE/scale (S^T) and -D with
+// D = sum_d dO * O (dP^T), each split in three bf16 parts at k = 0, 1, 2 of
+// the row (k = 3..15 zero); rows past Sq are all zero.  One warp per row.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const uint16_t* __restrict__ o,
                                                            const uint16_t* __restrict__ dout,
-                                                           float* __restrict__ dvec, int B, int H,
-                                                           int Sq) {
+                                                           const float* __restrict__ lse,
+                                                           uint8_t* __restrict__ bias, int B,
+                                                           int H, int Sq, float scale) {
+  const int nq = (Sq + kBN - 1) / kBN;
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (row >= static_cast<long long>(B) * Sq * H) return;
+  if (row >= static_cast<long long>(B) * H * nq * kBN) return;  // row = (b*H + h) * nq*128 + q
   const int lane = threadIdx.x & 31;
-  const int h = static_cast<int>(row % H);
-  const long long bq = row / H;
-  const int q = static_cast<int>(bq % Sq);
-  const int b = static_cast<int>(bq / Sq);
-  constexpr int PER = D / 32;  // 2 or 4 elements per lane
-  float acc = 0.0f;
-  const uint16_t* a = o + row * D + lane * PER;
-  const uint16_t* c = dout + row * D + lane * PER;
+  const int q = static_cast<int>(row % (static_cast<long long>(nq) * kBN));
+  const long long bh = row / (static_cast<long long>(nq) * kBN);
+  const int h = static_cast<int>(bh % H);
+  const int b = static_cast<int>(bh / H);
+  float dsum = 0.0f, nls = 0.0f;
+  if (q < Sq) {
+    constexpr int PER = D / 32;  // 2 or 4 elements per lane
+    const long long orow = (static_cast<long long>(b) * Sq + q) * H + h;
+    const uint16_t* a = o + orow * D + lane * PER;
+    const uint16_t* c = dout + orow * D + lane * PER;
 #pragma unroll
-  for (int i = 0; i < PER; i += 2) {
-    float x0, x1, y0, y1;
-    unpack2<BF16>(*reinterpret_cast<const uint32_t*>(a + i), x0, x1);
-    unpack2<BF16>(*reinterpret_cast<const uint32_t*>(c + i), y0, y1);
-    acc = fmaf(x0, y0, fmaf(x1, y1, acc));
+    for (int i = 0; i < PER; i += 2) {
+      float x0, x1, y0, y1;
+      unpack2<BF16>(*reinterpret_cast<const uint32_t*>(a + i), x0, x1);
+      unpack2<BF16>(*reinterpret_cast<const uint32_t*>(c + i), y0, y1);
+      dsum = fmaf(x0, y0, fmaf(x1, y1, dsum));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+    nls = -lse[bh * Sq + q] / scale;
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) dvec[(static_cast<long long>(b) * H + h) * Sq + q] = acc;
+  if (lane == 0) {
+    uint8_t* const t = bias + (bh * nq + q / kBN) * 2 * kBiasBytes;
+    const int r = q % kBN;
+    uint16_t sp[kBiasParts], dp[kBiasParts];
+    split3_bf16(q < Sq ? nls : 0.0f, sp);
+    split3_bf16(q < Sq ? -dsum : 0.0f, dp);
+    *reinterpret_cast<uint4*>(t + bias_offset(r, 0)) =
+        make_uint4(sp[0] | (static_cast<uint32_t>(sp[1]) << 16), sp[2], 0u, 0u);
+    *reinterpret_cast<uint4*>(t + bias_offset(r, 8)) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(t + kBiasBytes + bias_offset(r, 0)) =
+        make_uint4(dp[0] | (static_cast<uint32_t>(dp[1]) << 16), dp[2], 0u, 0u);
+    *reinterpret_cast<uint4*>(t + kBiasBytes + bias_offset(r, 8)) = make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 // dQ[b, q, h, :] = scale * acc[b, h, q, :] in the input dtype.
@@ -609,13 +660,15 @@ __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const float* __restr
 
 template <int D, bool BF16>
 cudaError_t launch_bwd(const BwdParams& p, const uint16_t* o, const uint16_t* dout,
-                       float* dvec, uint16_t* dq, int grid, cudaStream_t stream) {
+                       const float* lse, uint8_t* bias, uint16_t* dq, int grid,
+                       cudaStream_t stream) {
   const long long rows = static_cast<long long>(p.B) * p.Sq * p.H;
   cudaError_t e = cudaMemsetAsync(p.dq_acc, 0, static_cast<size_t>(rows) * D * sizeof(float),
                                   stream);
   if (e != cudaSuccess) return e;
-  attn_bwd_pre_kernel<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-      o, dout, dvec, p.B, p.H, p.Sq);
+  const long long prow = static_cast<long long>(p.B) * p.H * ((p.Sq + kBN - 1) / kBN) * kBN;
+  attn_bwd_pre_kernel<D, BF16><<<static_cast<unsigned>((prow + 7) / 8), 256, 0, stream>>>(
+      o, dout, lse, bias, p.B, p.H, p.Sq, p.scale);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const void* fn = reinterpret_cast<const void*>(&attn_bwd_kernel<D, BF16>);
