@@ -109,6 +109,22 @@ int encode_rows_heads_dim(CUtensorMap* m, const void* ptr, long long rows, int H
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// The backward's fp32 dQ accumulator [B*H, Sq, D] as a 3-D map {D, Sq, B*H}
+// with 32 x 128 x 1 boxes (128 B inner extent) and 128-byte swizzle: the
+// target of the per-step TMA reduce-adds.
+int encode_dq_acc(CUtensorMap* m, float* ptr, int BH, int Sq, int D) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Sq),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4,
+                           static_cast<cuuint64_t>(Sq) * static_cast<cuuint64_t>(D) * 4};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace attn
 
@@ -506,6 +522,7 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
       encode_rows_heads_dim(&p.tm_v, v, rows_k, H, D, bf16) != ATTN_OK)
     return ATTN_ERR_CUDA;
   p.dq_acc = static_cast<float*>(workspace);
+  if (encode_dq_acc(&p.tm_dq, p.dq_acc, B * H, Sq, D) != ATTN_OK) return ATTN_ERR_CUDA;
   uint8_t* bias = static_cast<uint8_t*>(workspace) + bwd_acc_bytes(B, H, Sq, D);
   p.bias = bias;
   p.dk = dk;

@@ -16,9 +16,9 @@
 //   TMEM columns: S^T | dP^T | dV | dK (128, 128, D, D); dQ of a step is
 //   written over dP^T once dS^T has been consumed, so S^T of the next query
 //   tile can be computed while this step's dS is still being formed.
-//   * warp 9 (one lane): TMA for the unit's K and V tiles and, per step
+//   * warp 13 (one lane): TMA for the unit's K and V tiles and, per step
 //     (128 queries), Q and dO tiles into a 2-stage ring;
-//   * warp 8 (one lane): tcgen05.mma
+//   * warp 12 (one lane): tcgen05.mma
 //       S^T  = K Q^T      (SS, K-major / K-major)
 //       dP^T = V dO^T     (SS)
 //       dV  += P^T dO     (TS: P^T from TMEM, dO MN-major)
@@ -29,12 +29,18 @@
 //     three-part bf16 split of each term (per query tile, written by the
 //     pre-pass), so S^T arrives as S^T - LSE/scale and dP^T as dP^T - D and
 //     the per-element loops below need no per-column loads;
-//   * warps 0-3: one thread per key (TMEM lane): P^T = 2^(scale log2e S'^T)
-//     written back as 16-bit over S^T, then dS^T = P^T dP'^T written as 16-bit
-//     over dP^T and into the dO stage (whose dO the dV and dP^T products have
-//     finished reading), as the A operand of dQ;
-//   * warps 4-7: one thread per query row: dQ of each step is added with
-//     fp32 atomics to a [B, H, Sq, D] accumulator; at the end of the unit they
+//   * warps 0-7: two threads per key (TMEM lane; warps w and w + 4 share lane
+//     quarter w), each for 64 of the step's 128 queries: P^T = 2^(scale log2e
+//     S'^T) written back as 16-bit into its own half's columns of S^T, then
+//     dS^T = P^T dP'^T into its half's columns of dP^T and into the dO stage
+//     (whose dO the dV and dP^T products have finished reading), as the A
+//     operand of dQ.  Half h writes only columns 64h .. 64h + 31, which it has
+//     already read, so the halves never wait for each other;
+//   * warps 8-11: one thread per query row: dQ of each step is staged in the
+//     step's Q and dO ring stages (free once dQ is computed; 128-byte
+//     swizzled, so the row-per-thread writes hit distinct banks) and added to
+//     an fp32 [B, H, Sq, D] accumulator by TMA tensor reduce-adds, after which
+//     the stages go back to the loader; at the end of the unit these warps
 //     write dK (times scale) and dV.
 // Every wait is bounded (same error word and abort flag as the forward).
 #pragma once
@@ -49,10 +55,11 @@ namespace bwd {
 
 constexpr int kBM = 128;  // keys per unit
 constexpr int kBN = 128;  // queries per step
-constexpr int kThreads = 320;
-constexpr int kDqWarp0 = 4;
-constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp = 9;
+constexpr int kThreads = 448;  // 14 warps: at most 4 per SM sub-partition, so <= 128 registers
+constexpr int kDsWarps = 8;
+constexpr int kDqWarp0 = 8;
+constexpr int kMmaWarp = 12;
+constexpr int kLoadWarp = 13;
 constexpr int kTmemCols = 512;
 // A 128 x 16 16-bit operand without swizzle: 8 x 8 core matrices of 8 rows x
 // 16 B; row r, element k at (r / 8) * 256 + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2.
@@ -61,6 +68,7 @@ constexpr int kBiasParts = 3;  // a term is the sum of three bf16 values
 
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // [B*S, H, D] 16-bit, box 64 x 1 x 128, 128-B swizzle
+  CUtensorMap tm_dq;                     // dq_acc as [B*H, Sq, D] fp32, box 32 x 128 x 1, 128-B swizzle
   const uint8_t* bias;                   // [B*H][query tile][2][kBiasBytes]: -LSE/scale, -D
   float* dq_acc;                         // [B, H, Sq, D] fp32, zero on entry
   void* dk;                              // [B, Sk, H, D]
@@ -84,8 +92,18 @@ struct BLayout {
   static constexpr int kBiasOff = kOnesOff + kBiasBytes;   // 2 stages x (S bias, D bias)
   static constexpr int kBarOff = kBiasOff + 2 * 2 * kBiasBytes;
   enum : int {
-    KVF = 0, KVE, QF0, QF1, QE0, QE1, SF, DPF, PR, DVD, DSR, DQF, DQE, OF, AE, DONE, kNumBars
+    KVF = 0, KVE, QF0, QF1, QE0, QE1, SF, DPF, PR, DVD, DSR, DQF, DQE, OF, AE, STG, DONE,
+    kNumBars
   };
+  // dQ staging (fp32, 128 rows x 32 columns = one 16 KiB swizzled box each):
+  // boxes 0, 1 in the step's Q stage, boxes 2, 3 in its dO stage (D = 128);
+  // both boxes of D = 64 in the dO stage.
+  static constexpr int kDqBox = 16384;
+  __host__ __device__ static constexpr int dq_box_off(int st, int j) {
+    return D == 128 ? (j < 2 ? kQOff + st * kTile + j * kDqBox
+                             : kDoOff + st * kDoStage + (j - 2) * kDqBox)
+                    : kDoOff + st * kDoStage + j * kDqBox;
+  }
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -118,6 +136,25 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar) : "memory");
 }
 
+// TMA tensor reduce-add of one box from shared memory into global fp32.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int c0,
+                                                  int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%1, %2, %3}], [%4];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {  // sources of all committed groups read
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {   // all committed groups complete
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __host__ __device__ constexpr int bias_offset(int r, int k) {
   return (r / 8) * 256 + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2;
 }
@@ -135,12 +172,6 @@ __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
-}
-
-// dst[0..3] += v (fp32, relaxed, no return value: the warp does not wait)
-__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
-  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
-               ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
 template <bool BF16>
@@ -204,10 +235,12 @@ __device__ void ds_role(const BwdParams& p, uint32_t tmem, uint8_t* base, uint32
   using L = BLayout<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int r = warp * 32 + lane;  // key row of this thread = TMEM lane
-  const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t tS = tmem + lane_bits + L::kColS;
-  const uint32_t tDP = tmem + lane_bits + L::kColDP;
+  const int quarter = warp & 3;
+  const int half = warp >> 2;           // queries 64 half .. 64 half + 63 of the step
+  const int r = quarter * 32 + lane;    // key row of this thread = TMEM lane
+  const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
+  const uint32_t tS = tmem + lane_bits + L::kColS + 64 * half;    // S^T, P^T of this half
+  const uint32_t tDP = tmem + lane_bits + L::kColDP + 64 * half;  // dP^T, dS^T of this half
   auto bar = [&](int i) { return bars + 8u * i; };
   const uint64_t c2 = ptx::f2(p.scale_log2, p.scale_log2);
 
@@ -217,19 +250,19 @@ __device__ void ds_role(const BwdParams& p, uint32_t tmem, uint8_t* base, uint32
     const BUnit w = cur.w;
     const int i = w.i0 + cur.j;
     const int key = w.kt * kBM + r;
-    const int qb = i * kBN;
+    const int qb = i * kBN + 64 * half;
     // columns c (query qb + c) visible to this key: c >= cmin and qb + c < Sq
     const int cmin = p.causal ? key - qb : 0;
     const int cmax = p.Sq - qb - 1;
     const bool row_ok = key < p.Sk;
-    const bool full = row_ok && cmin <= 0 && cmax >= kBN - 1;
+    const bool full = row_ok && cmin <= 0 && cmax >= 63;
 
     // ---- P^T = 2^(scale log2e (S^T - LSE / scale)), 16-bit, over S^T
     if (!wait_bar_warp(bar(L::SF), g & 1u, ctl)) return;
     ptx::tc_fence_after();
-    uint32_t pk[64];
+    uint32_t pk[32];
 #pragma unroll
-    for (int c0 = 0; c0 < kBN; c0 += 32) {
+    for (int c0 = 0; c0 < 64; c0 += 32) {
       uint32_t s[32];
       ptx::tmem_ld_x32(tS + c0, s);
 #pragma unroll
@@ -258,9 +291,9 @@ __device__ void ds_role(const BwdParams& p, uint32_t tmem, uint8_t* base, uint32
     if (!wait_bar_warp(bar(L::DPF), g & 1u, ctl)) return;
     if (!wait_bar_warp(bar(L::DVD), g & 1u, ctl)) return;  // dO of this stage consumed
     ptx::tc_fence_after();
-    uint8_t* const ds_tile = base + L::kDoOff + (g & 1u) * L::kDoStage;
+    uint8_t* const ds_tile = base + L::kDoOff + (g & 1u) * L::kDoStage + half * L::kBlk;
 #pragma unroll
-    for (int c0 = 0; c0 < kBN; c0 += 32) {
+    for (int c0 = 0; c0 < 64; c0 += 32) {
       uint32_t dp[32];
       ptx::tmem_ld_x32(tDP + c0, dp);
       uint32_t dk[16];
@@ -275,12 +308,12 @@ __device__ void ds_role(const BwdParams& p, uint32_t tmem, uint8_t* base, uint32
         dk[c / 2] = ptx::pack2<BF16>(a, b);
       }
       tmem_st_x16(tDP + c0 / 2, dk);
-      // shared memory: row r (key), queries c0 .. c0+31 = 4 chunks of 16 B in the
-      // 128-B swizzled block of queries 64 * (c0 / 64) .. +63
-      uint8_t* const row = ds_tile + (c0 >> 6) * L::kBlk + r * 128;
+      // shared memory: row r (key), queries 64 half + c0 .. +31 = 4 chunks of
+      // 16 B in the 128-B swizzled block of this half's 64 queries
+      uint8_t* const row = ds_tile + r * 128;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
-        const int chunk = ((c0 & 63) >> 3) + q4;
+        const int chunk = (c0 >> 3) + q4;
         *reinterpret_cast<uint4*>(row + ((chunk ^ (r & 7)) << 4)) =
             make_uint4(dk[4 * q4], dk[4 * q4 + 1], dk[4 * q4 + 2], dk[4 * q4 + 3]);
       }
@@ -295,7 +328,8 @@ __device__ void ds_role(const BwdParams& p, uint32_t tmem, uint8_t* base, uint32
 
 // -------------------------------------------------- dQ and the dK/dV epilogue
 template <int D, bool BF16>
-__device__ void dq_role(const BwdParams& p, uint32_t tmem, uint32_t bars, const Ctl& ctl) {
+__device__ void dq_role(const BwdParams& p, uint32_t tmem, uint32_t smem, uint8_t* base,
+                        uint32_t bars, const Ctl& ctl) {
   using L = BLayout<D>;
   const int warp = threadIdx.x >> 5;
   const int quarter = warp & 3;
@@ -323,21 +357,33 @@ __device__ void dq_role(const BwdParams& p, uint32_t tmem, uint32_t bars, const 
     for (int j = 0; j < w.n; ++j, ++g) {
       if (!wait_bar_warp(bar(L::DQF), g & 1u, ctl)) return;
       ptx::tc_fence_after();
-      uint32_t v[D];
-      if constexpr (D == 128) {
-        ptx::tmem_ld_x128(tmem + lane_bits + L::kColDP, v);
-      } else {
-        ptx::tmem_ld_x64(tmem + lane_bits + L::kColDP, v);
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(L::DQE));
-      const int q = (w.i0 + j) * kBN + r;
-      if (q < p.Sq) {
-        float* dst = p.dq_acc + ((static_cast<long long>(w.b) * p.H + w.h) * p.Sq + q) * D;
+      const uint32_t st = g & 1u;
 #pragma unroll
-        for (int c = 0; c < D / 4; ++c)
-          red_add_v4(dst + 4 * c, __uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                     __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld_x32(tmem + lane_bits + L::kColDP + c0, v);
+        if (c0 + 32 >= D) {  // dQ fully read: the dP^T columns are free
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(L::DQE));
+        }
+        // row r of box c0 / 32: 8 chunks of 16 B, swizzled
+        uint8_t* const row = base + L::dq_box_off(st, c0 / 32) + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) =
+              make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+      }
+      fence_proxy_async_smem();
+      ptx::mbar_arrive(bar(L::STG));
+      if (threadIdx.x == kDqWarp0 * 32) {  // one thread moves the tile and frees the stages
+        if (!wait_bar(bar(L::STG), g & 1u, ctl)) return;
+        const int q0 = (w.i0 + j) * kBN, bh = w.b * p.H + w.h;
+#pragma unroll
+        for (int b = 0; b < D / 32; ++b)
+          tma_reduce_add_3d(&p.tm_dq, smem + L::dq_box_off(st, b), 32 * b, q0, bh);
+        bulk_commit();
+        bulk_wait_read();
+        ptx::mbar_arrive(bar(L::QE0 + st));
       }
     }
     // ---- dK (times scale) and dV of this key tile
@@ -437,8 +483,8 @@ __device__ void mma_loop(const BwdParams& p, uint32_t smem, uint32_t tmem, uint3
       ptx::tc_fence_after();
       const uint64_t dDo_mn = ptx::desc_sw128(dobase, L::kBlk, 1024);
 #pragma unroll
-      for (int ks = 0; ks < kBN / 16; ++ks)  // dV += P^T dO
-        ptx::mma_ts(tDV, tS + ks * 8, dDo_mn + ((ks * 2048) >> 4), kIdAcc,
+      for (int ks = 0; ks < kBN / 16; ++ks)  // dV += P^T dO (P^T of half h at 64 h)
+        ptx::mma_ts(tDV, tS + (ks >> 2) * 64 + (ks & 3) * 8, dDo_mn + ((ks * 2048) >> 4), kIdAcc,
                     (j > 0 || ks > 0) ? 1u : 0u);
       ptx::mma_commit(bar(L::DVD));
       if (j + 1 < w.n && !issue_s(g + 1)) return;  // next query tile of this unit
@@ -447,15 +493,14 @@ __device__ void mma_loop(const BwdParams& p, uint32_t smem, uint32_t tmem, uint3
       const uint64_t dQ_mn = ptx::desc_sw128(qbase, L::kBlk, 1024);
       const uint64_t dDs_mn = ptx::desc_sw128(dobase, L::kBlk, 1024);
 #pragma unroll
-      for (int ks = 0; ks < kBN / 16; ++ks)  // dK += dS^T Q
-        ptx::mma_ts(tDK, tDP + ks * 8, dQ_mn + ((ks * 2048) >> 4), kIdAcc,
-                    (j > 0 || ks > 0) ? 1u : 0u);
+      for (int ks = 0; ks < kBN / 16; ++ks)  // dK += dS^T Q (dS^T of half h at 64 h)
+        ptx::mma_ts(tDK, tDP + (ks >> 2) * 64 + (ks & 3) * 8, dQ_mn + ((ks * 2048) >> 4),
+                    kIdAcc, (j > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
       for (int ks = 0; ks < kBM / 16; ++ks)  // dQ = dS K (over this tile's keys)
         ptx::mma_ss(tDP, dDs_mn + ((ks * 2048) >> 4), dK_mn + ((ks * 2048) >> 4), kIdDq,
                     ks > 0 ? 1u : 0u);
-      ptx::mma_commit(bar(L::DQF));
-      ptx::mma_commit(bar(L::QE0 + st));
+      ptx::mma_commit(bar(L::DQF));  // the dQ warps release the stage after staging dQ
       if (j == w.n - 1) {
         ptx::mma_commit(bar(L::OF));
         ptx::mma_commit(bar(L::KVE));
@@ -504,7 +549,7 @@ __device__ void load_loop(const BwdParams& p, uint32_t smem, uint32_t bars, cons
 }
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __maxnreg__(128) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
   using L = BLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -518,8 +563,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
-      const bool many = i == L::PR || i == L::DSR || i == L::DQE || i == L::AE;
-      ptx::mbar_init(bars + 8u * i, many ? 128u : 1u);
+      const uint32_t count = (i == L::PR || i == L::DSR) ? 32u * kDsWarps
+                             : (i == L::DQE || i == L::AE || i == L::STG) ? 128u
+                                                                            : 1u;
+      ptx::mbar_init(bars + 8u * i, count);
     }
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -548,10 +595,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   const uint32_t tmem = *tmem_slot;
   const Ctl ctl{abort_flag, p.err, p.timeout_ns};
 
-  if (warp < kDqWarp0) {
+  if (warp < kDsWarps) {
     ds_role<D, BF16>(p, tmem, base, bars, ctl);
   } else if (warp < kMmaWarp) {
-    dq_role<D, BF16>(p, tmem, bars, ctl);
+    dq_role<D, BF16>(p, tmem, smem, base, bars, ctl);
+    if (threadIdx.x == kDqWarp0 * 32) bulk_wait_all();  // every reduce-add landed
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       mma_loop<D, BF16>(p, smem, tmem, bars, ctl);
