@@ -37,11 +37,13 @@
 //     operand of dQ.  Half h writes only columns 64h .. 64h + 31, which it has
 //     already read, so the halves never wait for each other;
 //   * warps 8-11: one thread per query row: dQ of each step is staged in the
-//     step's Q and dO ring stages (free once dQ is computed; 128-byte
-//     swizzled, so the row-per-thread writes hit distinct banks) and added to
-//     an fp32 [B, H, Sq, D] accumulator by TMA tensor reduce-adds, after which
-//     the stages go back to the loader; at the end of the unit these warps
-//     write dK (times scale) and dV.
+//     step's dO ring stage (free once dQ is computed; 128-byte swizzled, so
+//     the row-per-thread writes hit distinct banks; 64 columns at a time) and
+//     added to an fp32 [B, H, Sq, D] accumulator by TMA tensor reduce-adds,
+//     after which the dO stage goes back to the loader.  The Q stage has its
+//     own barriers and returns to the loader as soon as dQ is computed, so the
+//     next Q tile is not held up by the reduce-adds.  At the end of the unit
+//     these warps write dK (times scale) and dV.
 // Every wait is bounded (same error word and abort flag as the forward).
 #pragma once
 
@@ -91,18 +93,17 @@ struct BLayout {
   static constexpr int kOnesOff = kDoOff + 2 * kDoStage;  // 128 x 16 ones column (bf16)
   static constexpr int kBiasOff = kOnesOff + kBiasBytes;   // 2 stages x (S bias, D bias)
   static constexpr int kBarOff = kBiasOff + 2 * 2 * kBiasBytes;
+  // QF/QE: Q tile + S bias of a ring stage; DOF/DOE: dO tile + D bias (and
+  // later dS, then the dQ staging) of a ring stage.
   enum : int {
-    KVF = 0, KVE, QF0, QF1, QE0, QE1, SF, DPF, PR, DVD, DSR, DQF, DQE, OF, AE, STG, DONE,
-    kNumBars
+    KVF = 0, KVE, QF0, QF1, QE0, QE1, DOF0, DOF1, DOE0, DOE1, SF, DPF, PR, DVD, DSR, DQF, DQE,
+    OF, AE, STG, STF, DONE, kNumBars
   };
-  // dQ staging (fp32, 128 rows x 32 columns = one 16 KiB swizzled box each):
-  // boxes 0, 1 in the step's Q stage, boxes 2, 3 in its dO stage (D = 128);
-  // both boxes of D = 64 in the dO stage.
+  // dQ staging: fp32, 128 rows x 32 columns = one 16 KiB swizzled box; two
+  // boxes (64 columns) at a time in the step's dO stage.
   static constexpr int kDqBox = 16384;
-  __host__ __device__ static constexpr int dq_box_off(int st, int j) {
-    return D == 128 ? (j < 2 ? kQOff + st * kTile + j * kDqBox
-                             : kDoOff + st * kDoStage + (j - 2) * kDqBox)
-                    : kDoOff + st * kDoStage + j * kDqBox;
+  __host__ __device__ static constexpr int dq_box_off(int st, int pos) {
+    return kDoOff + st * kDoStage + pos * kDqBox;
   }
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag
   static constexpr int kBytes = kMiscOff + 16;
@@ -339,7 +340,7 @@ __device__ void dq_role(const BwdParams& p, uint32_t tmem, uint32_t smem, uint8_
   auto bar = [&](int i) { return bars + 8u * i; };
   uint16_t* const DK = static_cast<uint16_t*>(p.dk);
   uint16_t* const DV = static_cast<uint16_t*>(p.dv);
-  uint32_t g = 0, u_cnt = 0;
+  uint32_t g = 0, u_cnt = 0, stg_n = 0, stf_n = 0;
   BUnit w;
   for (int k = 0; bwd_unit(p, k, w); ++k) {
     const int key = w.kt * kBM + r;
@@ -358,33 +359,55 @@ __device__ void dq_role(const BwdParams& p, uint32_t tmem, uint32_t smem, uint8_
       if (!wait_bar_warp(bar(L::DQF), g & 1u, ctl)) return;
       ptx::tc_fence_after();
       const uint32_t st = g & 1u;
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_x32(tmem + lane_bits + L::kColDP + c0, v);
-        if (c0 + 32 >= D) {  // dQ fully read: the dP^T columns are free
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(bar(L::DQE));
-        }
-        // row r of box c0 / 32: 8 chunks of 16 B, swizzled
-        uint8_t* const row = base + L::dq_box_off(st, c0 / 32) + r * 128;
+      const bool issuer = threadIdx.x == kDqWarp0 * 32;
+      const int q0 = (w.i0 + j) * kBN, bh = w.b * p.H + w.h;
+      auto stage_box = [&](int pos, const uint32_t (&v)[32]) {  // row r of a box, swizzled
+        uint8_t* const row = base + L::dq_box_off(st, pos) + r * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) =
               make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+      };
+      // the issuer waits until all 128 rows are staged, reduces the two boxes
+      // of columns x0 .. x0+63, and waits until they have been read
+      auto flush = [&](int x0) -> bool {
+        fence_proxy_async_smem();
+        ptx::mbar_arrive(bar(L::STG));
+        if (issuer) {
+          if (!wait_bar(bar(L::STG), stg_n & 1u, ctl)) return false;
+          tma_reduce_add_3d(&p.tm_dq, smem + L::dq_box_off(st, 0), x0, q0, bh);
+          tma_reduce_add_3d(&p.tm_dq, smem + L::dq_box_off(st, 1), x0 + 32, q0, bh);
+          bulk_commit();
+          bulk_wait_read();
+        }
+        ++stg_n;
+        return true;
+      };
+      uint32_t v0[32], v1[32];
+      ptx::tmem_ld_x32(tmem + lane_bits + L::kColDP, v0);
+      ptx::tmem_ld_x32(tmem + lane_bits + L::kColDP + 32, v1);
+      if constexpr (D == 64) {
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::DQE));  // dQ fully read: the dP^T columns are free
+        stage_box(0, v0);
+        stage_box(1, v1);
+        if (!flush(0)) return;
+      } else {
+        stage_box(0, v0);
+        stage_box(1, v1);
+        ptx::tmem_ld_x32(tmem + lane_bits + L::kColDP + 64, v0);
+        ptx::tmem_ld_x32(tmem + lane_bits + L::kColDP + 96, v1);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::DQE));  // dQ fully read: the dP^T columns are free
+        if (!flush(0)) return;
+        if (issuer) ptx::mbar_arrive(bar(L::STF));  // the staging boxes may be reused
+        if (!wait_bar_warp(bar(L::STF), stf_n & 1u, ctl)) return;
+        ++stf_n;
+        stage_box(0, v0);
+        stage_box(1, v1);
+        if (!flush(64)) return;
       }
-      fence_proxy_async_smem();
-      ptx::mbar_arrive(bar(L::STG));
-      if (threadIdx.x == kDqWarp0 * 32) {  // one thread moves the tile and frees the stages
-        if (!wait_bar(bar(L::STG), g & 1u, ctl)) return;
-        const int q0 = (w.i0 + j) * kBN, bh = w.b * p.H + w.h;
-#pragma unroll
-        for (int b = 0; b < D / 32; ++b)
-          tma_reduce_add_3d(&p.tm_dq, smem + L::dq_box_off(st, b), 32 * b, q0, bh);
-        bulk_commit();
-        bulk_wait_read();
-        ptx::mbar_arrive(bar(L::QE0 + st));
-      }
+      if (issuer) ptx::mbar_arrive(bar(L::DOE0 + st));  // the dO stage goes back to the loader
     }
     // ---- dK (times scale) and dV of this key tile
     if (!wait_bar_warp(bar(L::OF), u_cnt & 1u, ctl)) return;
@@ -467,6 +490,7 @@ __device__ void mma_loop(const BwdParams& p, uint32_t smem, uint32_t tmem, uint3
       const uint32_t qbase = smem + L::kQOff + st * L::kTile;
       const uint32_t dobase = smem + L::kDoOff + st * L::kDoStage;
       if (g > 0 && !wait_bar(bar(L::DQE), (g - 1) & 1u, ctl)) return;  // dP^T columns free
+      if (!wait_bar(bar(L::DOF0 + st), (g >> 1) & 1u, ctl)) return;     // dO and D bias here
       ptx::tc_fence_after();
       const uint64_t dDo_kmaj = ptx::desc_sw128(dobase, 16, 1024);
 #pragma unroll
@@ -500,7 +524,8 @@ __device__ void mma_loop(const BwdParams& p, uint32_t smem, uint32_t tmem, uint3
       for (int ks = 0; ks < kBM / 16; ++ks)  // dQ = dS K (over this tile's keys)
         ptx::mma_ss(tDP, dDs_mn + ((ks * 2048) >> 4), dK_mn + ((ks * 2048) >> 4), kIdDq,
                     ks > 0 ? 1u : 0u);
-      ptx::mma_commit(bar(L::DQF));  // the dQ warps release the stage after staging dQ
+      ptx::mma_commit(bar(L::DQF));
+      ptx::mma_commit(bar(L::QE0 + st));  // Q and the S bias no longer read
       if (j == w.n - 1) {
         ptx::mma_commit(bar(L::OF));
         ptx::mma_commit(bar(L::KVE));
@@ -530,20 +555,27 @@ __device__ void load_loop(const BwdParams& p, uint32_t smem, uint32_t bars, cons
     ++kv_cnt;
     for (int j = 0; j < w.n; ++j, ++g) {
       const uint32_t st = g & 1u;
-      if (g >= 2 && !wait_bar(bar(L::QE0 + st), ((g >> 1) - 1) & 1u, ctl)) return;
-      ptx::mbar_arrive_expect_tx(bar(L::QF0 + st), 2 * L::kTile + 2 * kBiasBytes);
       const int qrow = w.b * p.Sq + (w.i0 + j) * kBN;
       const int nq = (p.Sq + kBN - 1) / kBN;
       const long long tile = (static_cast<long long>(w.b) * p.H + w.h) * nq + w.i0 + j;
+      // Q tile and S bias
+      if (g >= 2 && !wait_bar(bar(L::QE0 + st), ((g >> 1) - 1) & 1u, ctl)) return;
+      ptx::mbar_arrive_expect_tx(bar(L::QF0 + st), L::kTile + kBiasBytes);
       bulk_load(smem + L::kBiasOff + st * 2 * kBiasBytes, p.bias + tile * 2 * kBiasBytes,
-                2 * kBiasBytes, bar(L::QF0 + st));
+                kBiasBytes, bar(L::QF0 + st));
 #pragma unroll
-      for (int blk = 0; blk < D / 64; ++blk) {
+      for (int blk = 0; blk < D / 64; ++blk)
         ptx::tma_load_3d(smem + L::kQOff + st * L::kTile + blk * L::kBlk, &p.tm_q,
                          bar(L::QF0 + st), blk * 64, w.h, qrow);
+      // dO tile and D bias
+      if (g >= 2 && !wait_bar(bar(L::DOE0 + st), ((g >> 1) - 1) & 1u, ctl)) return;
+      ptx::mbar_arrive_expect_tx(bar(L::DOF0 + st), L::kTile + kBiasBytes);
+      bulk_load(smem + L::kBiasOff + (st * 2 + 1) * kBiasBytes,
+                p.bias + tile * 2 * kBiasBytes + kBiasBytes, kBiasBytes, bar(L::DOF0 + st));
+#pragma unroll
+      for (int blk = 0; blk < D / 64; ++blk)
         ptx::tma_load_3d(smem + L::kDoOff + st * L::kDoStage + blk * L::kBlk, &p.tm_do,
-                         bar(L::QF0 + st), blk * 64, w.h, qrow);
-      }
+                         bar(L::DOF0 + st), blk * 64, w.h, qrow);
     }
   }
 }
@@ -615,6 +647,7 @@ __global__ void __maxnreg__(128) attn_bwd_kernel(const __grid_constant__ BwdPara
     for (uint32_t st = 0; st < 2 && st < g; ++st) {
       const uint32_t last = st + ((g - 1 - st) / 2) * 2;
       wait_bar(bars + 8u * (L::QF0 + st), (last >> 1) & 1u, ctl, false);
+      wait_bar(bars + 8u * (L::DOF0 + st), (last >> 1) & 1u, ctl, false);
     }
   }
 
