@@ -142,6 +142,12 @@ def peaks():
     return FALLBACK_PEAK_TFLOPS, "fallback (1.9 PFLOP/s bf16, earlier GB300 measurement)"
 
 
+def fp8_peak():
+    """Dense e4m3 peak: the measured bf16 peak times the nominal fp8/bf16 ratio (4.5/2.25)."""
+    bf, src = peaks()
+    return 2.0 * bf, src + " x 2 (nominal fp8 / bf16 dense ratio)"
+
+
 def hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -156,6 +162,7 @@ KERNEL_SOURCES = {
     "attn_fwd_kernel": ("ptx.cuh", "fwd_kernel.cuh"),
     "attn_decode_kernel": ("ptx.cuh", "fwd_kernel.cuh", "decode_kernel.cuh"),
     "attn_bwd_kernel": ("ptx.cuh", "fwd_kernel.cuh", "bwd_kernel.cuh"),
+    "attn_fwd_fp8_kernel": ("ptx.cuh", "fwd_kernel.cuh", "fwd_fp8_kernel.cuh"),
 }
 
 
@@ -227,6 +234,9 @@ def workload_info(wl):
         cfg.update(window=list(wl.window), global_q=wl.global_q)
     if wl.backward:
         cfg.update(backward=True)
+    if wl.fp8:  # Q, K, V are 1 byte; O 16-bit, LSE fp32
+        nbytes = tokens * wl.H * wl.D * (3 + 2) + tokens * wl.H * 4
+        cfg.update(fp8="e4m3, per-tensor scales", algorithmic_bytes_per_step=nbytes)
     return flops, nbytes, cfg
 
 
@@ -451,18 +461,25 @@ def main(argv=None):
     inp = W.make_inputs(wl, pin=True)
     q_h, k_h, v_h = inp["q"], inp["k"], inp["v"]
     do_h = inp.get("do")
+    if wl.fp8:  # e4m3 codes (1 byte) and one scale per tensor
+        (q_h, qs), (k_h, ks), (v_h, vs) = (W.quantize_e4m3(t) for t in (q_h, k_h, v_h))
+        q_h, k_h, v_h = (t.view(torch.uint8).pin_memory() for t in (q_h, k_h, v_h))
     cu_h = inp["cu_seqlens_q"]
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         q, k, v = (t.to(dev, non_blocking=True) for t in (q_h, k_h, v_h))
         cu = cu_h.to(dev) if cu_h is not None else None
-        o = torch.empty_like(q)
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev) if wl.fp8 \
+            else torch.empty_like(q)
         lse_shape = (wl.H, q.shape[0]) if wl.varlen else (wl.B, wl.H, wl.Sq)
         lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
         ws_dec = None
         if wl.decode:
             need = pkg.decode_workspace_bytes(wl.B, wl.H, wl.Sq, wl.Sk, wl.D)
             ws_dec = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        if wl.fp8:
+            ws_fp8 = torch.empty(pkg.fp8_workspace_bytes(wl.B, wl.H, wl.Sk, wl.D),
+                                 dtype=torch.uint8, device=dev)
         if wl.backward:  # O and LSE of the forward, computed once outside the timing
             dout = do_h.to(dev, non_blocking=True)
             pkg.attn_fwd(q, k, v, causal=wl.causal, scale=wl.scale, out=o, lse=lse,
@@ -473,6 +490,10 @@ def main(argv=None):
     torch.cuda.synchronize()
 
     def step():
+        if wl.fp8:
+            pkg.attn_fwd_fp8(q, k, v, q_scale=qs, k_scale=ks, v_scale=vs, causal=wl.causal,
+                             scale=wl.scale, workspace=ws_fp8, out=o, lse=lse, stream=stream)
+            return
         if wl.backward:
             pkg.attn_bwd(q, k, v, o, dout, lse, causal=wl.causal, scale=wl.scale,
                          workspace=ws_bwd, dq=dq_t, dk=dk_t, dv=dv_t, stream=stream)
@@ -493,6 +514,8 @@ def main(argv=None):
         raise SystemExit(f"device status {pkg.status_string(st)}")
     grid, smem = pkg.last_launch()
     launches_per_step = 3 if wl.backward else 1  # backward: D pre-pass, main, dQ conversion
+    if wl.fp8:
+        launches_per_step = 2  # V transpose, attention
     if wl.decode and pkg.decode_workspace_bytes(wl.B, wl.H, wl.Sq, wl.Sk, wl.D) > 0:
         launches_per_step = 2  # the split decode kernel and the merge kernel
     sampler = ClockSampler(local)
@@ -582,6 +605,11 @@ def main(argv=None):
         if wl.backward:
             kern = "attn_bwd_kernel"
             metric = "attention bwd TFLOP/s"
+        if wl.fp8:
+            peak, peak_src = fp8_peak()
+            achieved = flops / (kernel_ms * 1e-3) / 1e12
+            kern = "attn_fwd_fp8_kernel"
+            metric = "attention fwd fp8 TFLOP/s"
     traffic = profiled_traffic(wl.name, kern)
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
@@ -593,7 +621,8 @@ def main(argv=None):
         "metric": metric, "value": per_step / (ms_step * 1e-3),
         "unit": unit, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "fp16",
+        "vs_baseline": None,
+        "dtype": "e4m3" if wl.fp8 else ("bf16" if wl.dtype == "bf16" else "fp16"),
         "data": "synthetic", "config": cfg,
         "pct_of_peak": achieved / peak,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,

@@ -200,6 +200,31 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
 int attn_bwd_workspace(int B, int H, int Sq, int D, size_t* bytes);
 
 /*
+ * attn_fwd_fp8 -- attn_fwd for 8-bit (e4m3) Q, K, V with per-tensor scales.
+ *
+ * Low-precision operands as a memory and throughput lever of the fused kernel
+ * (page "深度学习算子优化：从TFLOPS幻觉到FlashAttention实战", §3).  The inputs are
+ * e4m3 codes (OCP FP8, 1-4-3, no infinities) and the real values are
+ * q = q_code * q_scale, k = k_code * k_scale, v = v_code * v_scale; O and LSE
+ * are those of attn_fwd on these real values, O in out_dtype (fp16/bf16).
+ * The probabilities are rounded to e4m3 for the P V product (the rounding
+ * largely cancels against the row sum, which adds the same rounded values).
+ * Dense layouts only: q [B, Sq, H, 128], k, v [B, Sk, H, 128] (1 byte each),
+ * o [B, Sq, H, 128] (out_dtype), lse float [B, H, Sq]; D must be 128
+ * (ATTN_ERR_UNSUPPORTED otherwise); causal as attn_fwd; all scales finite.
+ * workspace: device scratch of at least attn_fwd_fp8_workspace(B, H, Sk, 128)
+ * bytes (V transposed to [H, 128, keys], keys padded to a multiple of 16),
+ * 256-byte aligned.  Errors and ownership as attn_fwd; asynchronous on `stream`.
+ */
+int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                 int H, int Sq, int Sk, int D, float scale, float q_scale, float k_scale,
+                 float v_scale, int causal, void* workspace, size_t workspace_bytes,
+                 int out_dtype, void* stream);
+
+/* attn_fwd_fp8_workspace -- bytes of workspace attn_fwd_fp8 needs: H * 128 * B * round16(Sk). */
+int attn_fwd_fp8_workspace(int B, int H, int Sk, int D, size_t* bytes);
+
+/*
  * attn_check -- synchronise `stream`, then report and clear the device error
  * word of the current device: ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT,
  * ATTN_ERR_BAD_SEQLENS, or ATTN_ERR_CUDA if the stream itself failed.

@@ -18,11 +18,13 @@ from ._binding import (  # noqa: F401
     attn_check,
     attn_decode,
     attn_fwd,
+    attn_fwd_fp8,
     attn_fwd_raw,
     attn_fwd_window_raw,
     attn_merge,
     bwd_workspace_bytes,
     decode_workspace_bytes,
+    fp8_workspace_bytes,
     last_launch,
     load_library,
     num_sms,

@@ -30,7 +30,7 @@ DTYPE_CODES = {torch.float16: 0, torch.bfloat16: 1}
 EXPORTED = ("attn_fwd", "attn_check", "attn_status_string", "attn_num_sms",
             "attn_last_launch", "attn_release", "attn_fwd_noalloc", "attn_fwd_window",
             "attn_fwd_decode", "attn_decode_workspace", "attn_merge", "attn_bwd",
-            "attn_bwd_workspace")
+            "attn_bwd_workspace", "attn_fwd_fp8", "attn_fwd_fp8_workspace")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -73,6 +73,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.attn_bwd.restype = i
         lib.attn_bwd_workspace.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
         lib.attn_bwd_workspace.restype = i
+        lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, f, f, f, i, vp,
+                                     ctypes.c_size_t, i, vp]
+        lib.attn_fwd_fp8.restype = i
+        lib.attn_fwd_fp8_workspace.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_fwd_fp8_workspace.restype = i
         lib.attn_check.argtypes = [vp]
         lib.attn_check.restype = i
         lib.attn_status_string.argtypes = [i]
@@ -347,6 +352,56 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv
+
+
+def fp8_workspace_bytes(B: int, H: int, Sk: int, D: int = 128) -> int:
+    """Workspace bytes attn_fwd_fp8 needs for these sizes."""
+    n = ctypes.c_size_t(0)
+    st = load_library().attn_fwd_fp8_workspace(B, H, Sk, D, ctypes.byref(n))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_fp8_workspace")
+    return int(n.value)
+
+
+def attn_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, q_scale: float = 1.0,
+                 k_scale: float = 1.0, v_scale: float = 1.0, causal: bool = False,
+                 scale: Optional[float] = None, out_dtype=torch.bfloat16,
+                 workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                 lse: Optional[torch.Tensor] = None, stream=None):
+    """Attention forward on e4m3 inputs (dense, head dim 128).  Returns (O, LSE).
+
+    q [B,Sq,H,128], k/v [B,Sk,H,128] as torch.float8_e4m3fn (or uint8 codes); the
+    real values are code * scale per tensor.  O is ``out_dtype`` (bf16/fp16).
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous() or t.element_size() != 1:
+            raise ValueError(f"{name} must be a contiguous 1-byte (e4m3) CUDA tensor")
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape:
+        raise ValueError("q [B,Sq,H,D], k/v [B,Sk,H,D]")
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    if k.shape != (B, Sk, H, D):
+        raise ValueError("k/v shape mismatch")
+    if out_dtype not in DTYPE_CODES:
+        raise ValueError("out_dtype must be fp16 or bf16")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        need = fp8_workspace_bytes(B, H, Sk, D)
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        if out is None:
+            out = torch.empty((B, Sq, H, D), dtype=out_dtype, device=q.device)
+        if lse is None:
+            lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+        st = load_library().attn_fwd_fp8(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Sq,
+            Sk, D, ctypes.c_float(scale), ctypes.c_float(q_scale), ctypes.c_float(k_scale),
+            ctypes.c_float(v_scale), 1 if causal else 0, workspace.data_ptr(), workspace.numel(),
+            DTYPE_CODES[out_dtype], _stream_handle(stream) or None)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_fp8")
+    return out, lse
 
 
 def attn_check(stream=None) -> int:

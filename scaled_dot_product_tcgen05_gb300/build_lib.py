@@ -22,7 +22,8 @@ LIB_PATH = os.path.join(PKG, LIB_NAME)
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "noalloc.cu", "fwd_d64_f16.cu", "fwd_d64_bf16.cu", "fwd_d128_f16.cu",
-           "fwd_d128_bf16.cu", "decode_d64.cu", "decode_d128.cu", "bwd_d64.cu", "bwd_d128.cu"]
+           "fwd_d128_bf16.cu", "decode_d64.cu", "decode_d128.cu", "bwd_d64.cu", "bwd_d128.cu",
+           "fwd_fp8.cu"]
 
 
 def _nvcc() -> str:

@@ -16,6 +16,7 @@
 #include "attn.h"
 #include "bwd_kernel.cuh"
 #include "decode_kernel.cuh"
+#include "fwd_fp8_kernel.cuh"
 #include "launch.cuh"
 #include "merge_kernel.cuh"
 
@@ -554,6 +555,128 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   }
   t_last_grid = grid;
   t_last_smem = D == 64 ? bwd::BLayout<64>::kAlloc : bwd::BLayout<128>::kAlloc;
+  return ATTN_OK;
+}
+
+// -------------------------------------------------------------- fp8 (e4m3)
+namespace attn {
+namespace fp8 {
+extern template cudaError_t launch_fwd_fp8<true>(const Fp8Params&, const uint8_t*, uint8_t*, int,
+                                                 cudaStream_t);
+extern template cudaError_t launch_fwd_fp8<false>(const Fp8Params&, const uint8_t*, uint8_t*,
+                                                  int, cudaStream_t);
+}  // namespace fp8
+namespace {
+int fp8_sk_pad(int Sk) { return (Sk + 15) / 16 * 16; }
+// [rows, H, 128] e4m3 tensor, box 128 elements (128 B) x 1 head x 128 rows.
+int encode_e4m3_rows(CUtensorMap* m, const void* ptr, long long rows, int H) {
+  cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(H) * 128};
+  cuuint32_t box[3] = {128, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+// V^T [H, 128, keys] e4m3 (keys innermost), box 128 keys x 128 dims x 1 head.
+int encode_e4m3_vt(CUtensorMap* m, const void* ptr, long long keys, int H) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(keys), 128, static_cast<cuuint64_t>(H)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(keys), static_cast<cuuint64_t>(keys) * 128};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+}  // namespace
+}  // namespace attn
+
+extern "C" int attn_fwd_fp8_workspace(int B, int H, int Sk, int D, size_t* bytes) {
+  if (!bytes) return ATTN_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (B < 0 || H < 1 || Sk < 1) return ATTN_ERR_INVALID_ARG;
+  if (D != 128) return ATTN_ERR_UNSUPPORTED;
+  *bytes = static_cast<size_t>(H) * 128 * static_cast<size_t>(B) * fp8_sk_pad(Sk);
+  return ATTN_OK;
+}
+
+extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int H, int Sq, int Sk, int D, float scale, float q_scale,
+                            float k_scale, float v_scale, int causal, void* workspace,
+                            size_t workspace_bytes, int out_dtype, void* stream) {
+  // ---- argument checks (no CUDA call before these pass)
+  if (B < 0 || H < 1 || Sq < 0 || Sk < 1) return ATTN_ERR_INVALID_ARG;
+  if (D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (out_dtype != ATTN_DTYPE_FP16 && out_dtype != ATTN_DTYPE_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale) || !std::isfinite(q_scale) || !std::isfinite(k_scale) ||
+      !std::isfinite(v_scale))
+    return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || Sq == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || !aligned(workspace, 256))
+    return ATTN_ERR_MISALIGNED;
+  const long long rows_q = static_cast<long long>(B) * Sq;
+  const long long sk_pad = fp8_sk_pad(Sk);
+  const long long keys_t = static_cast<long long>(B) * sk_pad;
+  if (rows_q > INT_MAX - 2 * kUnitRows || keys_t > INT_MAX - 2 * kBN) return ATTN_ERR_INVALID_ARG;
+  const long long units = static_cast<long long>(B) * H * ((Sq + kUnitRows - 1) / kUnitRows);
+  if (units > INT_MAX / 2) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(workspace_bytes) < static_cast<long long>(H) * 128 * keys_t)
+    return ATTN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  DeviceState* ds = nullptr;
+  int st = device_state(dev, &ds);
+  if (st != ATTN_OK) return st;
+  const void* ptrs[] = {q, k, v, o, lse, workspace};
+  for (const void* ptr : ptrs)
+    if (!on_device(ptr, dev)) return ATTN_ERR_INVALID_ARG;
+
+  fp8::Fp8Params q8;
+  FwdParams& p = q8.f;
+  if (encode_e4m3_rows(&p.tm_q, q, rows_q, H) != ATTN_OK ||
+      encode_e4m3_rows(&p.tm_k, k, static_cast<long long>(B) * Sk, H) != ATTN_OK ||
+      encode_e4m3_vt(&p.tm_v, workspace, keys_t, H) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+  p.o = o;
+  p.lse = lse;
+  p.cu_q = nullptr;
+  p.cu_k = nullptr;
+  p.err = ds->err;
+  p.B = B;
+  p.H = H;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.varlen = 0;
+  set_mask(p, causal, -1, -1, 0);
+  const double c = static_cast<double>(scale) * q_scale * k_scale;
+  p.scale_log2 = static_cast<float>(c * 1.4426950408889634);
+  p.scale_pos = c > 0.0 ? 1 : 0;
+  p.timeout_ns = timeout_ns_from_env();
+  q8.sk_pad = static_cast<int>(sk_pad);
+  q8.o_mul = v_scale;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int grid = static_cast<int>(units < ds->sms ? units : ds->sms);
+  const uint8_t* v8 = static_cast<const uint8_t*>(v);
+  uint8_t* vt = static_cast<uint8_t*>(workspace);
+  const cudaError_t e = out_dtype == ATTN_DTYPE_BF16
+                            ? fp8::launch_fwd_fp8<true>(q8, v8, vt, grid, s)
+                            : fp8::launch_fwd_fp8<false>(q8, v8, vt, grid, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  t_last_grid = grid;
+  t_last_smem = fp8::Layout8::kAlloc;
   return ATTN_OK;
 }
 

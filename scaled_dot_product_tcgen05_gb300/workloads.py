@@ -47,6 +47,7 @@ class Workload:
     global_q: int = 0               # leading query rows that ignore the window
     decode: bool = False            # Sq new queries against a full KV cache of Sk rows
     backward: bool = False          # gradients dQ, dK, dV from a seeded dO
+    fp8: bool = False               # Q, K, V quantised per tensor to e4m3 (dtype = output)
 
     @property
     def windowed(self) -> bool:
@@ -79,6 +80,7 @@ def standard_workloads() -> dict:
                 (the query and the 4095 before it) with 64 global query rows: the
                 128K-context hybrid of page "长文本处理性能断层真相", §2.5
     8 backward  B=1 H=32 S=16384 D=128 bf16 causal: dQ, dK, dV from a seeded dO
+    9 fp8       the long 64K causal problem with Q, K, V quantised to e4m3 (bf16 output)
     7 decode    KV-cache decode (page "长文本处理性能断层真相", §2.2): one new token
                 per sequence against a 128K-token cache (B=1 H=32 D=128 bf16), and
                 a batch of 16 sequences with 32K-token caches and 4 new tokens each
@@ -98,6 +100,8 @@ def standard_workloads() -> dict:
     w["long128k_causal"] = _wl("long128k_causal", 5, 1, 32, 131072, 128, "bf16", True, draw=2)
     w["window128k_causal"] = _wl("window128k_causal", 6, 1, 32, 131072, 128, "bf16", True,
                                  window=(4095, 0), global_q=64)
+    w["fp8_long64k_causal"] = _wl("fp8_long64k_causal", 9, 1, 32, 65536, 128, "bf16", True,
+                                  fp8=True)
     w["bwd16k_causal"] = _wl("bwd16k_causal", 8, 1, 32, 16384, 128, "bf16", True, backward=True)
     w["decode128k_q1"] = Workload(name="decode128k_q1", wid=7, B=1, H=32, Sq=1, Sk=131072,
                                   D=128, dtype="bf16", causal=True, decode=True)
@@ -224,3 +228,16 @@ def window_flops(B: int, H: int, Sq: int, Sk: int, D: int, causal: bool, window=
                  global_q: int = 0) -> float:
     """4 * D FLOPs per visible (query, key) pair, summed over rows, heads and batch."""
     return 4.0 * D * B * H * float(visible_key_counts(Sq, Sk, causal, window, global_q).sum())
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor e4m3 codes of a tensor and their scale (x ~ code * scale).
+
+    The scale maps the largest magnitude to 448 (the e4m3 maximum); codes are
+    torch's float8_e4m3fn rounding (nearest even).  Input generation only: the
+    attention math sees the codes and the scale.
+    """
+    amax = float(x.abs().max()) if x.numel() else 1.0
+    scale = (amax / 448.0) if amax > 0 else 1.0
+    codes = (x.float() / scale).to(torch.float8_e4m3fn)
+    return codes, scale

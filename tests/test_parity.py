@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 WL = W.standard_workloads()
 # workloads the oracle checks in full (the long-context ones are sampled below)
 SMALL = [n for n, w in WL.items()
-         if w.Sq <= 4096 and not w.windowed and not w.decode and not w.backward]
+         if w.Sq <= 4096 and not w.windowed and not w.decode and not w.backward and not w.fp8]
 
 
 @pytest.fixture(scope="module", autouse=True)
