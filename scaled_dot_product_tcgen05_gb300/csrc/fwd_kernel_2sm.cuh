@@ -169,21 +169,21 @@ __device__ __forceinline__ bool softmax_half_step(uint32_t tS, uint32_t tP, uint
   const float alpha = rescale ? ptx::ex2(st.m - m_safe) : 1.0f;
   st.m = m_use;
 
-  const uint64_t cl2 = ptx::f2(cle, cle);
-  const uint64_t nm2 = ptx::f2(-m_safe, -m_safe);
-  uint64_t lx0 = ptx::f2(0.f, 0.f), lx1 = lx0;
+  const float nm = -m_safe;
+  float la = 0.f, lb = 0.f, lc = 0.f, ld = 0.f;
   float lp0 = 0.f, lp1 = 0.f, lp2 = 0.f, lp3 = 0.f;
   uint32_t pk[32];
 #pragma unroll
   for (int c = 0; c < 64; c += 4) {
-    float x0, x1, x2, x3;
-    ptx::f2_split(ptx::f2_fma(ptx::f2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), cl2,
-                              nm2), x0, x1);
-    ptx::f2_split(ptx::f2_fma(ptx::f2(__uint_as_float(r[c + 2]), __uint_as_float(r[c + 3])),
-                              cl2, nm2), x2, x3);
+    const float x0 = fmaf(__uint_as_float(r[c]), cle, nm);
+    const float x1 = fmaf(__uint_as_float(r[c + 1]), cle, nm);
+    const float x2 = fmaf(__uint_as_float(r[c + 2]), cle, nm);
+    const float x3 = fmaf(__uint_as_float(r[c + 3]), cle, nm);
     const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1), p2 = ptx::ex2(x2), p3 = ptx::ex2(x3);
-    lx0 = ptx::f2_add(lx0, ptx::f2(p0, p1));
-    lx1 = ptx::f2_add(lx1, ptx::f2(p2, p3));
+    la += p0;
+    lb += p1;
+    lc += p2;
+    ld += p3;
     pk[c / 2] = ptx::pack2<BF16>(p0, p1);
     pk[c / 2 + 1] = ptx::pack2<BF16>(p2, p3);
     // the denominator sums the same 16-bit values the P.V product sees
@@ -193,10 +193,7 @@ __device__ __forceinline__ bool softmax_half_step(uint32_t tS, uint32_t tP, uint
     lp3 = ptx::add_hi16<BF16>(lp3, pk[c / 2 + 1]);
   }
   ptx::tmem_st_x32(tP, pk);
-  float a0, a1, b0, b1;
-  ptx::f2_split(lx0, a0, a1);
-  ptx::f2_split(lx1, b0, b1);
-  st.l_x = st.l_x * alpha + ((a0 + a1) + (b0 + b1));
+  st.l_x = st.l_x * alpha + ((la + lb) + (lc + ld));
   st.l_p = st.l_p * alpha + ((lp0 + lp1) + (lp2 + lp3));
 
   if (!first && __any_sync(0xffffffffu, rescale)) {
