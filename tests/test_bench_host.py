@@ -79,3 +79,49 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--workload", "tiny_causal"], capture_output=True, text=True, env=env,
                        timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_workload_info_for_the_extension_workloads():
+    from scaled_dot_product_tcgen05_gb300 import workloads as W
+    wls = W.standard_workloads()
+    # sliding window: the exact count of visible (query, key) pairs
+    wl = wls["window128k_causal"]
+    f, _, cfg = bench.workload_info(wl)
+    S, Wn, G = 131072, 4096, 64
+    pairs = sum(min(i + 1, Wn) for i in range(S))  # G <= W: global rows see i + 1 keys too
+    assert f == 4.0 * 128 * 32 * pairs and cfg["window"] == [4095, 0] and cfg["global_q"] == G
+    # decode: bytes = K and V caches + q + o + lse; flops = 4 D per visible pair
+    wl = wls["decode32k_b16_q4"]
+    f, nb, cfg = bench.workload_info(wl)
+    assert nb == 16 * 32768 * 32 * 128 * 4 + 16 * 4 * 32 * 128 * 4 + 16 * 32 * 4 * 4
+    assert f == 4.0 * 128 * 16 * 32 * sum(32768 - 4 + t + 1 for t in range(4))
+    # backward: 2.5 x the forward convention; 8 tensors of bytes
+    wl = wls["bwd16k_causal"]
+    f, nb, cfg = bench.workload_info(wl)
+    assert f == 2.5 * 4 * 32 * 16384 ** 2 * 128 / 2 and cfg["backward"]
+    assert nb == 16384 * 32 * 128 * 2 * 8 + 16384 * 32 * 4
+    # fp8: the forward's flops, 1-byte inputs
+    wl = wls["fp8_long64k_causal"]
+    f, nb, cfg = bench.workload_info(wl)
+    assert f == 4 * 32 * 65536 ** 2 * 128 / 2
+    assert nb == 65536 * 32 * 128 * 5 + 65536 * 32 * 4 and cfg["fp8"].startswith("e4m3")
+
+
+def test_visible_key_counts_matches_a_direct_count():
+    from scaled_dot_product_tcgen05_gb300 import workloads as W
+    import numpy as np
+    for Sq, Sk, causal, win, g in [(9, 9, True, (2, 0), 0), (7, 11, False, (1, 3), 2),
+                                   (10, 10, False, (-1, -1), 0), (6, 6, True, (-1, -1), 0)]:
+        got = W.visible_key_counts(Sq, Sk, causal, win, g)
+        want = []
+        for i in range(Sq):
+            n = 0
+            for j in range(Sk):
+                ok = True
+                if i >= g:
+                    ok = (win[0] < 0 or j >= i - win[0]) and (win[1] < 0 or j <= i + win[1])
+                if causal and j > i:
+                    ok = False
+                n += ok
+            want.append(n)
+        assert np.array_equal(got, np.array(want))
