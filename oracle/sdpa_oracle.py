@@ -280,3 +280,35 @@ def attention_backward_dense(q, k, v, do, scale: float, causal: bool,
                                             scale, causal)
             dq[b, :, h], dk[b, :, h], dv[b, :, h] = g
     return dq, dk, dv
+
+
+def attention_backward_varlen(q, k, v, do, cu_seqlens_q, cu_seqlens_k, scale: float,
+                              causal: bool, heads: Optional[Sequence[int]] = None):
+    """Packed varlen batch: q/do [Tq,H,D], k/v [Tk,H,D] -> dQ, dK, dV in the same layouts.
+
+    Sequence b's queries cu_seqlens_q[b]:cu_seqlens_q[b+1] see only its keys
+    cu_seqlens_k[b]:cu_seqlens_k[b+1] (page "长文本处理性能断层真相", §1), so its
+    gradients are those of attention_backward_one_head on its slices.  A
+    sequence without queries gives its keys zero dK and dV; one without keys
+    gives its queries zero dQ.  Rows that belong to no sequence, and heads not
+    listed in ``heads``, are NaN.
+    """
+    q, k, v, do = (_as_f64(x) for x in (q, k, v, do))
+    cq = [int(x) for x in np.asarray(cu_seqlens_q).tolist()]
+    ck = [int(x) for x in np.asarray(cu_seqlens_k).tolist()]
+    dq = np.full(q.shape, np.nan)
+    dk = np.full(k.shape, np.nan)
+    dv = np.full(v.shape, np.nan)
+    H = q.shape[1]
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        for h in (range(H) if heads is None else heads):
+            if q1 == q0 or k1 == k0:
+                dq[q0:q1, h] = 0.0
+                dk[k0:k1, h] = 0.0
+                dv[k0:k1, h] = 0.0
+                continue
+            g = attention_backward_one_head(q[q0:q1, h], k[k0:k1, h], v[k0:k1, h],
+                                            do[q0:q1, h], scale, causal)
+            dq[q0:q1, h], dk[k0:k1, h], dv[k0:k1, h] = g
+    return dq, dk, dv

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 from oracle.sdpa_oracle import (attention_backward_dense, attention_backward_one_head,
-                                attention_one_head)
+                                attention_backward_varlen, attention_one_head)
 
 
 def _rng(seed):
@@ -155,3 +155,71 @@ def test_backward_mutant_is_caught(bug):
         except (AssertionError, ValueError, IndexError):
             caught.append(pin.__name__)
     assert caught, f"no pin catches the planted mistake {bug!r}"
+
+
+# ------------------------------------------------------------ packed sequences
+def test_varlen_equal_lengths_is_the_dense_batch():
+    """B sequences of one length packed back to back: the dense batch, bit for bit."""
+    r = _rng(31)
+    B, S, H, D = 3, 6, 2, 4
+    q, k, v, do = (r.normal(size=(B, S, H, D)) for _ in range(4))
+    cu = np.arange(0, (B + 1) * S, S, dtype=np.int32)
+    for causal in (False, True):
+        dense = attention_backward_dense(q, k, v, do, 0.4, causal)
+        packed = attention_backward_varlen(*(x.reshape(B * S, H, D) for x in (q, k, v, do)),
+                                           cu, cu, 0.4, causal)
+        for x, y in zip(dense, packed):
+            np.testing.assert_array_equal(x.reshape(B * S, H, D), y)
+
+
+def test_varlen_sequences_are_independent():
+    """Perturbing one sequence's inputs leaves every other sequence's gradients unchanged,
+    and each sequence's gradients are those of its own slices."""
+    r = _rng(32)
+    H, D = 2, 3
+    cq = np.array([0, 5, 5, 12, 15], dtype=np.int32)
+    ck = np.array([0, 4, 8, 8, 14], dtype=np.int32)
+    q, do = r.normal(size=(16, H, D)), r.normal(size=(16, H, D))   # row 15: no sequence
+    k, v = r.normal(size=(14, H, D)), r.normal(size=(14, H, D))
+    g = attention_backward_varlen(q, k, v, do, cq, ck, 0.7, True)
+    assert np.all(np.isnan(g[0][15]))
+    # sequence 1 has keys but no queries, sequence 2 queries but no keys
+    assert np.all(g[1][4:8] == 0) and np.all(g[2][4:8] == 0) and np.all(g[0][5:12] == 0)
+    k2, v2 = k.copy(), v.copy()
+    k2[8:14] += 3.0
+    v2[8:14] -= 2.0
+    g2 = attention_backward_varlen(q, k2, v2, do, cq, ck, 0.7, True)
+    for x, y in zip(g, g2):
+        np.testing.assert_array_equal(x[:5], y[:5])
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b:b + 2].tolist() + ck[b:b + 2].tolist()
+        if q1 == q0 or k1 == k0:
+            continue
+        for h in range(H):
+            ref = attention_backward_one_head(q[q0:q1, h], k[k0:k1, h], v[k0:k1, h],
+                                              do[q0:q1, h], 0.7, True)
+            for x, y in zip((g[0][q0:q1, h], g[1][k0:k1, h], g[2][k0:k1, h]), ref):
+                np.testing.assert_array_equal(x, y)
+
+
+def test_varlen_matches_torch_autograd_on_a_ragged_batch():
+    """The packed gradients equal torch autograd through a block-diagonal masked SDPA."""
+    r = _rng(33)
+    H, D = 2, 4
+    cq = np.array([0, 3, 9, 10], dtype=np.int32)
+    ck = np.array([0, 5, 9, 13], dtype=np.int32)
+    q, do = r.normal(size=(10, H, D)), r.normal(size=(10, H, D))
+    k, v = r.normal(size=(13, H, D)), r.normal(size=(13, H, D))
+    g = attention_backward_varlen(q, k, v, do, cq, ck, 0.5, True)
+    mask = np.zeros((10, 13), dtype=bool)
+    for b in range(3):
+        for i in range(cq[b], cq[b + 1]):
+            for j in range(ck[b], ck[b + 1]):
+                mask[i, j] = (j - ck[b]) <= (i - cq[b])
+    qt, kt, vt = (torch.tensor(x.transpose(1, 0, 2), requires_grad=True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt,
+                                                         attn_mask=torch.from_numpy(mask),
+                                                         scale=0.5)
+    o.backward(torch.from_numpy(do.transpose(1, 0, 2)))
+    for x, t in zip(g, (qt, kt, vt)):
+        np.testing.assert_allclose(x, t.grad.numpy().transpose(1, 0, 2), rtol=0, atol=1e-12)
