@@ -51,6 +51,8 @@ typedef enum { ATTN_DTYPE_FP16 = 0, ATTN_DTYPE_BF16 = 1 } attn_dtype;
  *     Sq / Sk are the TOTAL packed rows (the allocation lengths).  Sequence b
  *     owns query rows [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key rows
  *     [cu_seqlens_k[b], cu_seqlens_k[b+1]); it never attends to another one.
+ *     Rows that belong to no sequence are still read as padding of a
+ *     neighbour's tiles (with weight zero) and must hold finite values.
  *
  * Arguments:
  *   q, k, v   fp16 or bf16 (per dtype), 16-byte aligned device pointers.
@@ -175,29 +177,45 @@ int attn_merge(const void* o_parts, const float* lse_parts, int n_parts, int B, 
  * with P recomputed from the forward's LSE (P = exp(scale q.k - LSE)):
  *   dV = P^T dO,  dS = P * (dO V^T - D),  D = rowsum(dO * O),
  *   dQ = scale dS K,  dK = scale dS^T Q.
- * Dense layouts only (as attn_fwd without cu_seqlens):
- *   q, o, dout, dq   [B, Sq, H, D]     k, v, dk, dv  [B, Sk, H, D]   (dtype)
- *   lse              float [B, H, Sq]  the LSE attn_fwd returned for q, k, v
- * causal as attn_fwd (top-left).  D 64 or 128.  scale must be finite and
+ * Layouts as attn_fwd:
+ *   dense (cu_seqlens_q = cu_seqlens_k = NULL):
+ *     q, o, dout, dq   [B, Sq, H, D]     k, v, dk, dv  [B, Sk, H, D]   (dtype)
+ *     lse              float [B, H, Sq]
+ *   packed sequences (both cu_seqlens given, device int32 [B + 1], as attn_fwd):
+ *     q, o, dout, dq   [Sq, H, D]        k, v, dk, dv  [Sk, H, D]      (Sq, Sk: total rows)
+ *     lse              float [H, Sq]
+ * lse is the LSE attn_fwd returned for q, k, v.  causal as attn_fwd
+ * (top-left, within each sequence).  D 64 or 128.  scale must be finite and
  * non-zero (ATTN_ERR_UNSUPPORTED for 0: the LSE term is carried as -LSE/scale).
- * All 16-bit pointers 16-byte
- * aligned, lse 4-byte.  workspace: device scratch of at least
- * attn_bwd_workspace(B, H, Sq, D) bytes, 256-byte aligned (an fp32 dQ
- * accumulator and D); the call zeroes what it needs.  dQ is accumulated with
- * fp32 atomics, so its last bits may differ between runs; dK and dV are
+ * All 16-bit pointers 16-byte aligned, lse and cu_seqlens 4-byte.  workspace:
+ * device scratch of at least attn_bwd_workspace(B, H, Sq, D, packed) bytes
+ * (packed = 1 when cu_seqlens are given), 256-byte aligned; the call
+ * initialises what it needs.  As in attn_fwd, rows of q, k, v and dout that
+ * belong to no sequence must be finite (o and lse there are not read).  dq
+ * rows that belong to no sequence come out zero; dk/dv rows of keys that
+ * belong to no sequence are not written (with no query rows at all, Sq = 0,
+ * the whole of dk and dv is zeroed).  Malformed sequence bounds (cu_seqlens
+ * not non-decreasing within [0, Sq] / [0, Sk]) make the call do nothing
+ * further and attn_check report ATTN_ERR_BAD_SEQLENS.  dQ is accumulated with
+ * fp32 reduce-adds, so its last bits may differ between runs; dK and dV are
  * deterministic.  Errors and ownership as attn_fwd; asynchronous on `stream`.
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
              const float* lse, void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk,
-             int D, float scale, int causal, void* workspace, size_t workspace_bytes,
-             int dtype, void* stream);
+             int D, float scale, int causal, const int32_t* cu_seqlens_q,
+             const int32_t* cu_seqlens_k, void* workspace, size_t workspace_bytes, int dtype,
+             void* stream);
 
 /*
  * attn_bwd_workspace -- bytes of workspace attn_bwd needs: an fp32 dQ
- * accumulator (B*H*Sq*D*4, rounded up to 256) and 8 KiB per 128-query tile
- * per (sequence, head) for the per-query terms -LSE/scale and -D.
+ * accumulator (query rows * H * D * 4, rounded up to 256) and 8 KiB per
+ * 128-query tile per (sequence, head) for the per-query terms -LSE/scale and
+ * -D.  Dense (packed = 0): B * ceil(Sq / 128) tiles per head.  Packed
+ * (packed = 1; B sequences, Sq total query rows): at most
+ * floor((Sq + 127 B) / 128) tiles per head, plus 4 * (B + 2) bytes (rounded up
+ * to 256) for the per-sequence tile offsets.
  */
-int attn_bwd_workspace(int B, int H, int Sq, int D, size_t* bytes);
+int attn_bwd_workspace(int B, int H, int Sq, int D, int packed, size_t* bytes);
 
 /*
  * attn_fwd_fp8 -- attn_fwd for 8-bit (e4m3) Q, K, V with per-tensor scales.

@@ -68,10 +68,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.attn_decode_workspace.restype = i
         lib.attn_merge.argtypes = [vp, vp, i, i, i, i, i, vp, vp, i, vp]
         lib.attn_merge.restype = i
-        lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp,
-                                 ctypes.c_size_t, i, vp]
+        lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp,
+                                 vp, ctypes.c_size_t, i, vp]
         lib.attn_bwd.restype = i
-        lib.attn_bwd_workspace.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_bwd_workspace.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
         lib.attn_bwd_workspace.restype = i
         lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, f, f, f, i, vp,
                                      ctypes.c_size_t, i, vp]
@@ -302,10 +302,10 @@ def attn_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, *,
     return out, lse
 
 
-def bwd_workspace_bytes(B: int, H: int, Sq: int, D: int) -> int:
-    """Workspace bytes attn_bwd needs for these sizes."""
+def bwd_workspace_bytes(B: int, H: int, Sq: int, D: int, packed: bool = False) -> int:
+    """Workspace bytes attn_bwd needs (packed: B sequences, Sq total query rows)."""
     n = ctypes.c_size_t(0)
-    st = load_library().attn_bwd_workspace(B, H, Sq, D, ctypes.byref(n))
+    st = load_library().attn_bwd_workspace(B, H, Sq, D, 1 if packed else 0, ctypes.byref(n))
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd_workspace")
     return int(n.value)
@@ -313,32 +313,55 @@ def bwd_workspace_bytes(B: int, H: int, Sq: int, D: int) -> int:
 
 def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              dout: torch.Tensor, lse: torch.Tensor, *, causal: bool = False,
-             scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None,
-             dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
-             dv: Optional[torch.Tensor] = None, stream=None):
-    """Gradients (dQ, dK, dV) of :func:`attn_fwd` (dense layouts) from dO.
+             scale: Optional[float] = None, cu_seqlens_q: Optional[torch.Tensor] = None,
+             cu_seqlens_k: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None, dq: Optional[torch.Tensor] = None,
+             dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None, stream=None):
+    """Gradients (dQ, dK, dV) of :func:`attn_fwd` from dO, in the forward's layouts.
 
-    q, o, dout [B,Sq,H,D]; k, v [B,Sk,H,D]; lse fp32 [B,H,Sq] as returned by
-    attn_fwd for the same inputs.  ``workspace`` (uint8 CUDA tensor of at least
-    :func:`bwd_workspace_bytes`) is allocated when not given.
+    dense : q, o, dout [B,Sq,H,D]; k, v [B,Sk,H,D]; lse fp32 [B,H,Sq]
+    varlen: q, o, dout [Tq,H,D]; k, v [Tk,H,D]; int32 cu_seqlens [B+1]; lse [H,Tq]
+    ``lse`` is what attn_fwd returned for the same inputs.  ``workspace`` (uint8
+    CUDA tensor of at least :func:`bwd_workspace_bytes`) is allocated when not
+    given.
     """
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
         _check_16bit(name, t)
     if not (q.dtype == k.dtype == v.dtype == o.dtype == dout.dtype):
         raise ValueError("q, k, v, o, dout must share one dtype")
-    if q.dim() != 4 or k.dim() != 4:
-        raise ValueError("dense layouts only: q [B,Sq,H,D], k/v [B,Sk,H,D]")
-    B, Sq, H, D = q.shape
-    Sk = k.shape[1]
-    if k.shape != (B, Sk, H, D) or v.shape != k.shape or o.shape != q.shape or \
-            dout.shape != q.shape:
-        raise ValueError("shape mismatch")
-    if lse.shape != (B, H, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 tensor [B, H, Sq]")
+    varlen = cu_seqlens_q is not None or cu_seqlens_k is not None
+    if varlen:
+        if cu_seqlens_q is None or cu_seqlens_k is None:
+            raise ValueError("cu_seqlens_q and cu_seqlens_k must be given together")
+        if q.dim() != 3 or k.dim() != 3:
+            raise ValueError("varlen q/o/dout must be [Tq,H,D], k/v [Tk,H,D]")
+        Tq, H, D = q.shape
+        Tk = k.shape[0]
+        if k.shape != (Tk, H, D) or v.shape != k.shape or o.shape != q.shape or \
+                dout.shape != q.shape:
+            raise ValueError("shape mismatch")
+        for name, c in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+            if c.dtype != torch.int32 or not c.is_cuda or c.dim() != 1 or not c.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous int32 CUDA vector")
+        if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 1:
+            raise ValueError("cu_seqlens_q/k must both have B+1 entries")
+        B, Sq, Sk = cu_seqlens_q.numel() - 1, Tq, Tk
+        lse_shape, ws_args = (H, Tq), (B, H, Tq, D, True)
+    else:
+        if q.dim() != 4 or k.dim() != 4:
+            raise ValueError("dense layouts: q [B,Sq,H,D], k/v [B,Sk,H,D]")
+        B, Sq, H, D = q.shape
+        Sk = k.shape[1]
+        if k.shape != (B, Sk, H, D) or v.shape != k.shape or o.shape != q.shape or \
+                dout.shape != q.shape:
+            raise ValueError("shape mismatch")
+        lse_shape, ws_args = (B, H, Sq), (B, H, Sq, D)
+    if tuple(lse.shape) != lse_shape or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError(f"lse must be a contiguous fp32 tensor of shape {lse_shape}")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     with torch.cuda.device(q.device):
-        need = bwd_workspace_bytes(B, H, Sq, D)
+        need = bwd_workspace_bytes(*ws_args)
         if workspace is None:
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
         dq = torch.empty_like(q) if dq is None else dq
@@ -347,8 +370,10 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
         st = load_library().attn_bwd(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
             lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Sq, Sk, D,
-            ctypes.c_float(scale), 1 if causal else 0, workspace.data_ptr(), workspace.numel(),
-            DTYPE_CODES[q.dtype], _stream_handle(stream) or None)
+            ctypes.c_float(scale), 1 if causal else 0,
+            cu_seqlens_q.data_ptr() if varlen else None,
+            cu_seqlens_k.data_ptr() if varlen else None, workspace.data_ptr(),
+            workspace.numel(), DTYPE_CODES[q.dtype], _stream_handle(stream) or None)
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv

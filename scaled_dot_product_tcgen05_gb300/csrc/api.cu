@@ -110,14 +110,15 @@ int encode_rows_heads_dim(CUtensorMap* m, const void* ptr, long long rows, int H
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-// The backward's fp32 dQ accumulator [B*H, Sq, D] as a 3-D map {D, Sq, B*H}
-// with 32 x 128 x 1 boxes (128 B inner extent) and 128-byte swizzle: the
-// target of the per-step TMA reduce-adds.
-int encode_dq_acc(CUtensorMap* m, float* ptr, int BH, int Sq, int D) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Sq),
-                        static_cast<cuuint64_t>(BH)};
+// The backward's fp32 dQ accumulator [slices, rows, D] as a 3-D map {D, rows,
+// slices} with 32 x 128 x 1 boxes (128 B inner extent) and 128-byte swizzle:
+// the target of the per-step TMA reduce-adds.  Dense: slices = B*H, rows =
+// Sq; packed: slices = H, rows = all query rows.
+int encode_dq_acc(CUtensorMap* m, float* ptr, int slices, int rows, int D) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(slices)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4,
-                           static_cast<cuuint64_t>(Sq) * static_cast<cuuint64_t>(D) * 4};
+                           static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(D) * 4};
   cuuint32_t box[3] = {32, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
@@ -448,58 +449,76 @@ extern "C" int attn_merge(const void* o_parts, const float* lse_parts, int n_par
 // ---------------------------------------------------------------- backward
 namespace attn {
 namespace bwd {
-extern template cudaError_t launch_bwd<64, false>(const BwdParams&, const uint16_t*, const uint16_t*, const float*, uint8_t*, uint16_t*, int, cudaStream_t);
-extern template cudaError_t launch_bwd<64, true>(const BwdParams&, const uint16_t*, const uint16_t*, const float*, uint8_t*, uint16_t*, int, cudaStream_t);
-extern template cudaError_t launch_bwd<128, false>(const BwdParams&, const uint16_t*, const uint16_t*, const float*, uint8_t*, uint16_t*, int, cudaStream_t);
-extern template cudaError_t launch_bwd<128, true>(const BwdParams&, const uint16_t*, const uint16_t*, const float*, uint8_t*, uint16_t*, int, cudaStream_t);
+extern template cudaError_t launch_bwd<64, false>(const BwdParams&, const uint16_t*, const uint16_t*, const float*, uint8_t*, int32_t*, long long, uint16_t*, int, cudaStream_t);
+extern template cudaError_t launch_bwd<64, true>(const BwdParams&, const uint16_t*, const uint16_t*, const float*, uint8_t*, int32_t*, long long, uint16_t*, int, cudaStream_t);
+extern template cudaError_t launch_bwd<128, false>(const BwdParams&, const uint16_t*, const uint16_t*, const float*, uint8_t*, int32_t*, long long, uint16_t*, int, cudaStream_t);
+extern template cudaError_t launch_bwd<128, true>(const BwdParams&, const uint16_t*, const uint16_t*, const float*, uint8_t*, int32_t*, long long, uint16_t*, int, cudaStream_t);
 }  // namespace bwd
 namespace {
-// fp32 dQ accumulator, then the bias tiles of the two products (-LSE/scale
-// and -D, 2 x 4 KiB per 128-query tile).
-long long bwd_acc_bytes(int B, int H, int Sq, int D) {
-  return ((static_cast<long long>(B) * H * Sq * D * 4 + 255) / 256) * 256;
-}
-long long bwd_ws_bytes(int B, int H, int Sq, int D) {
-  const long long tiles = static_cast<long long>(B) * H * ((Sq + bwd::kBN - 1) / bwd::kBN);
-  return bwd_acc_bytes(B, H, Sq, D) + tiles * 2 * bwd::kBiasBytes;
+// The backward's workspace: an fp32 dQ accumulator, then the bias tiles of the
+// two products (-LSE/scale and -D, 2 x 4 KiB per 128-query tile and head),
+// then (packed sequences) the per-sequence tile offsets.  Dense: B*H*ceil(Sq/128)
+// tiles; packed (Sq = all query rows): at most floor((Sq + 127 B) / 128) per head.
+struct BwdWs {
+  long long acc, bias, tiles_bound, tiles, total;
+};
+BwdWs bwd_ws(int B, int H, int Sq, int D, bool varlen) {
+  BwdWs w;
+  const long long rows = varlen ? Sq : static_cast<long long>(B) * Sq;
+  w.acc = ((rows * H * D * 4 + 255) / 256) * 256;
+  w.tiles_bound = varlen ? (static_cast<long long>(Sq) + 127LL * B) / bwd::kBN
+                         : static_cast<long long>(B) * ((Sq + bwd::kBN - 1) / bwd::kBN);
+  w.bias = w.tiles_bound * H * 2 * bwd::kBiasBytes;
+  w.tiles = varlen ? ((static_cast<long long>(B) + 2) * 4 + 255) / 256 * 256 : 0;
+  w.total = w.acc + w.bias + w.tiles;
+  return w;
 }
 }  // namespace
 }  // namespace attn
 
-extern "C" int attn_bwd_workspace(int B, int H, int Sq, int D, size_t* bytes) {
+extern "C" int attn_bwd_workspace(int B, int H, int Sq, int D, int varlen, size_t* bytes) {
   if (!bytes) return ATTN_ERR_INVALID_ARG;
   *bytes = 0;
   if (B < 0 || H < 1 || Sq < 0) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  *bytes = static_cast<size_t>(bwd_ws_bytes(B, H, Sq, D));
+  *bytes = static_cast<size_t>(bwd_ws(B, H, Sq, D, varlen != 0).total);
   return ATTN_OK;
 }
 
 extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o,
                         const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
-                        int H, int Sq, int Sk, int D, float scale, int causal, void* workspace,
-                        size_t workspace_bytes, int dtype, void* stream) {
+                        int H, int Sq, int Sk, int D, float scale, int causal,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                        void* workspace, size_t workspace_bytes, int dtype, void* stream) {
   // ---- argument checks (no CUDA call before these pass)
   if (B < 0 || H < 1 || Sq < 0 || Sk < 1) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (dtype != ATTN_DTYPE_FP16 && dtype != ATTN_DTYPE_BF16) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (scale == 0.0f) return ATTN_ERR_UNSUPPORTED;  // the LSE term is carried as -LSE/scale
-  if (B == 0 || Sq == 0) return ATTN_OK;
+  const bool varlen = cu_seqlens_q != nullptr || cu_seqlens_k != nullptr;
+  if (varlen && (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0) return ATTN_OK;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
     return ATTN_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
       !aligned(lse, 4) || !aligned(workspace, 256))
     return ATTN_ERR_MISALIGNED;
-  const long long rows_q = static_cast<long long>(B) * Sq;
-  const long long rows_k = static_cast<long long>(B) * Sk;
+  if (varlen && (!aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4))) return ATTN_ERR_MISALIGNED;
+  const long long rows_q = varlen ? Sq : static_cast<long long>(B) * Sq;
+  const long long rows_k = varlen ? Sk : static_cast<long long>(B) * Sk;
   if (rows_q > INT_MAX - 2 * bwd::kBN || rows_k > INT_MAX - 2 * bwd::kBM)
     return ATTN_ERR_INVALID_ARG;
-  const long long units = static_cast<long long>(B) * H * ((Sk + bwd::kBM - 1) / bwd::kBM);
+  // unit indices are int: B*H*ceil(Sk/128) (dense) or H*(ceil(Sk/128)+B) (packed)
+  const long long units = varlen
+      ? static_cast<long long>(H) * ((rows_k + bwd::kBM - 1) / bwd::kBM + B)
+      : static_cast<long long>(B) * H * ((Sk + bwd::kBM - 1) / bwd::kBM);
   if (units > INT_MAX / 2) return ATTN_ERR_INVALID_ARG;
-  const long long need = bwd_ws_bytes(B, H, Sq, D);
-  if (static_cast<long long>(workspace_bytes) < need) return ATTN_ERR_INVALID_ARG;
+  const BwdWs wsl = bwd_ws(B, H, Sq, D, varlen);
+  if (wsl.tiles_bound * H * bwd::kBN / 8 > INT_MAX) return ATTN_ERR_INVALID_ARG;  // pre-pass grid
+  if (rows_q > 0 && static_cast<long long>(workspace_bytes) < wsl.total)
+    return ATTN_ERR_INVALID_ARG;
 
   // ---- device checks
   int dev = 0;
@@ -513,6 +532,18 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   const void* ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
   for (const void* ptr : ptrs)
     if (!on_device(ptr, dev)) return ATTN_ERR_INVALID_ARG;
+  if (varlen && (!on_device(cu_seqlens_q, dev) || !on_device(cu_seqlens_k, dev)))
+    return ATTN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (rows_q == 0) {  // no query sees any key: dK = dV = 0
+    const size_t bytes = static_cast<size_t>(rows_k) * H * D * 2;
+    if (cudaMemsetAsync(dk, 0, bytes, s) != cudaSuccess ||
+        cudaMemsetAsync(dv, 0, bytes, s) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    return ATTN_OK;
+  }
 
   // ---- parameters
   bwd::BwdParams p;
@@ -523,32 +554,42 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
       encode_rows_heads_dim(&p.tm_v, v, rows_k, H, D, bf16) != ATTN_OK)
     return ATTN_ERR_CUDA;
   p.dq_acc = static_cast<float*>(workspace);
-  if (encode_dq_acc(&p.tm_dq, p.dq_acc, B * H, Sq, D) != ATTN_OK) return ATTN_ERR_CUDA;
-  uint8_t* bias = static_cast<uint8_t*>(workspace) + bwd_acc_bytes(B, H, Sq, D);
+  if (encode_dq_acc(&p.tm_dq, p.dq_acc, varlen ? H : B * H, Sq, D) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+  uint8_t* bias = static_cast<uint8_t*>(workspace) + wsl.acc;
+  int32_t* tiles = varlen ? reinterpret_cast<int32_t*>(bias + wsl.bias) : nullptr;
   p.bias = bias;
+  p.tiles = tiles;
   p.dk = dk;
   p.dv = dv;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
   p.err = ds->err;
   p.B = B;
   p.H = H;
   p.Sq = Sq;
   p.Sk = Sk;
+  p.Tq = static_cast<int>(rows_q);
+  p.varlen = varlen ? 1 : 0;
   p.causal = causal ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = timeout_ns_from_env();
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int grid = static_cast<int>(units < ds->sms ? units : ds->sms);
+  const int grid = static_cast<int>(units < ds->sms ? (units > 0 ? units : 1) : ds->sms);
   const uint16_t* o16 = static_cast<const uint16_t*>(o);
   const uint16_t* do16 = static_cast<const uint16_t*>(dout);
   uint16_t* dq16 = static_cast<uint16_t*>(dq);
   cudaError_t e;
   if (D == 64)
-    e = bf16 ? bwd::launch_bwd<64, true>(p, o16, do16, lse, bias, dq16, grid, s)
-             : bwd::launch_bwd<64, false>(p, o16, do16, lse, bias, dq16, grid, s);
+    e = bf16 ? bwd::launch_bwd<64, true>(p, o16, do16, lse, bias, tiles, wsl.tiles_bound, dq16,
+                                         grid, s)
+             : bwd::launch_bwd<64, false>(p, o16, do16, lse, bias, tiles, wsl.tiles_bound, dq16,
+                                          grid, s);
   else
-    e = bf16 ? bwd::launch_bwd<128, true>(p, o16, do16, lse, bias, dq16, grid, s)
-             : bwd::launch_bwd<128, false>(p, o16, do16, lse, bias, dq16, grid, s);
+    e = bf16 ? bwd::launch_bwd<128, true>(p, o16, do16, lse, bias, tiles, wsl.tiles_bound,
+                                          dq16, grid, s)
+             : bwd::launch_bwd<128, false>(p, o16, do16, lse, bias, tiles, wsl.tiles_bound,
+                                           dq16, grid, s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_CUDA;

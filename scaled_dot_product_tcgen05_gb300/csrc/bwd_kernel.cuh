@@ -10,6 +10,9 @@
 // interface and states that masked connections carry no gradient; the
 // formulas are the chain rule through the forward definition.
 //
+// Sequences are either dense (B of Sq queries and Sk keys) or packed
+// (cu_seqlens, as the forward); every index below is within the sequence.
+//
 // GB300 mapping: a persistent kernel, one CTA per SM, work unit = (sequence,
 // head, 128-key tile).  Keys are the M dimension of every product the unit
 // accumulates, so dK and dV stay in tensor memory for the whole unit:
@@ -26,9 +29,9 @@
 //       dQ   = dS K       (SS: dS MN-major from shared memory, K MN-major)
 //   * the per-query terms -LSE/scale and -D enter the products themselves: one
 //     extra K = 16 step multiplies a ones column (in shared memory) by a
-//     three-part bf16 split of each term (per query tile, written by the
-//     pre-pass), so S^T arrives as S^T - LSE/scale and dP^T as dP^T - D and
-//     the per-element loops below need no per-column loads;
+//     three-part bf16 split of each term (16 bytes per query row, written by
+//     the pre-pass), so S^T arrives as S^T - LSE/scale and dP^T as dP^T - D
+//     and the per-element loops below need no per-column loads;
 //   * warps 0-7: two threads per key (TMEM lane; warps w and w + 4 share lane
 //     quarter w), each for 64 of the step's 128 queries: P^T = 2^(scale log2e
 //     S'^T) written back as 16-bit into its own half's columns of S^T, then
@@ -39,7 +42,7 @@
 //   * warps 8-11: one thread per query row: dQ of each step is staged in the
 //     step's dO ring stage (free once dQ is computed; 128-byte swizzled, so
 //     the row-per-thread writes hit distinct banks; 64 columns at a time) and
-//     added to an fp32 [B, H, Sq, D] accumulator by TMA tensor reduce-adds,
+//     added to an fp32 [H, rows, D] accumulator by TMA tensor reduce-adds,
 //     after which the dO stage goes back to the loader.  The Q stage has its
 //     own barriers and returns to the loader as soon as dQ is computed, so the
 //     next Q tile is not held up by the reduce-adds.  At the end of the unit
@@ -69,14 +72,23 @@ constexpr int kBiasBytes = 4096;
 constexpr int kBiasParts = 3;  // a term is the sum of three bf16 values
 
 struct BwdParams {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // [B*S, H, D] 16-bit, box 64 x 1 x 128, 128-B swizzle
-  CUtensorMap tm_dq;                     // dq_acc as [B*H, Sq, D] fp32, box 32 x 128 x 1, 128-B swizzle
-  const uint8_t* bias;                   // [B*H][query tile][2][kBiasBytes]: -LSE/scale, -D
-  float* dq_acc;                         // [B, H, Sq, D] fp32, zero on entry
-  void* dk;                              // [B, Sk, H, D]
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // [rows, H, D] 16-bit, box 64 x 1 x 128, 128-B swizzle
+  // dq_acc, fp32, box 32 x 128 x 1, 128-B swizzle: dense [B*H, Sq, D], packed [H, Tq, D]
+  CUtensorMap tm_dq;
+  // per 128-query tile t of (sequence b, head h): [2][kBiasBytes] (-LSE/scale,
+  // -D), t = tile0(b) * H + h * nq(b) + i, tile0(b) = the tiles of sequences
+  // before b (dense: b * nq)
+  const uint8_t* bias;
+  const int32_t* tiles;                  // packed: tile0(0..B) and a valid-bounds flag
+  float* dq_acc;                         // zero on entry
+  void* dk;                              // [key rows, H, D]
   void* dv;
+  const int32_t* cu_q;                   // packed sequences only
+  const int32_t* cu_k;
   int* err;
-  int B, H, Sq, Sk, causal;
+  int B, H, Sq, Sk;  // dense: per-sequence lengths; packed: total rows
+  int Tq;            // query rows in all: B * Sq dense, Sq packed
+  int varlen, causal;
   float scale, scale_log2;
   long long timeout_ns;
 };
@@ -189,20 +201,81 @@ __device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
 
 // Work unit u -> (b, h, key tile kt); units of one head are consecutive, key
 // tiles in increasing order (under causal the first key tiles see the most
-// query tiles).  Steps: query tiles i0 .. nq-1.
+// query tiles).  Steps: query tiles i0 .. nq-1 of the sequence.
 struct BUnit {
   int b, h, kt, i0, n;
+  int q_start, Lq, k_start, Lk;  // the sequence's first rows and lengths
+  int tile0;                     // bias tiles of the sequences before b, per head
+  int base, units;               // packed: first unit of sequence b and its unit count
 };
 
-__device__ __forceinline__ bool bwd_unit(const BwdParams& p, int k, BUnit& w) {
-  const int nk = (p.Sk + kBM - 1) / kBM;
+// Packed sequences: sequence w.b's rows, lengths and unit count into w.
+__device__ __forceinline__ void bwd_load_seq(const BwdParams& p, BUnit& w, bool report) {
+  w.units = 0;
+  w.q_start = w.Lq = w.k_start = w.Lk = 0;
+  if (w.b >= p.B) return;
+  const int q0 = __ldg(p.cu_q + w.b), q1 = __ldg(p.cu_q + w.b + 1);
+  const int k0 = __ldg(p.cu_k + w.b), k1 = __ldg(p.cu_k + w.b + 1);
+  const bool ok = 0 <= q0 && q0 <= q1 && q1 <= p.Sq && 0 <= k0 && k0 <= k1 && k1 <= p.Sk;
+  if (!ok) {  // the sequence is skipped and the call reports ATTN_ERR_BAD_SEQLENS
+    if (report) atomicOr(p.err, kErrBadSeqlens);
+    return;
+  }
+  w.q_start = q0;
+  w.Lq = q1 - q0;
+  w.k_start = k0;
+  w.Lk = k1 - k0;
+  w.tile0 = __ldg(p.tiles + w.b);
+  w.units = p.H * ((w.Lk + kBM - 1) / kBM);
+}
+
+// Before the first bwd_unit call of a role.
+template <bool VARLEN>
+__device__ __forceinline__ void bwd_walk(const BwdParams& p, BUnit& w, bool report) {
+  w.b = 0;
+  w.base = 0;
+  if constexpr (VARLEN) {
+    if (__ldg(p.tiles + p.B + 1) == 0) {  // malformed bounds somewhere: no work at all
+      w.b = p.B;
+      w.units = 0;
+      return;
+    }
+    bwd_load_seq(p, w, report);
+  }
+}
+
+// The k-th unit of this CTA (dealt as the forward deals its units); packed
+// sequences are walked forward, so k must increase from call to call.
+template <bool VARLEN>
+__device__ __forceinline__ bool bwd_unit(const BwdParams& p, int k, BUnit& w,
+                                         bool report = false) {
   const int u = unit_of(k);
-  if (u >= p.B * p.H * nk) return false;
-  const int bh = u / nk;
-  w.kt = u - bh * nk;
-  w.b = bh / p.H;
-  w.h = bh - w.b * p.H;
-  const int nq = (p.Sq + kBN - 1) / kBN;
+  if constexpr (!VARLEN) {
+    const int nk = (p.Sk + kBM - 1) / kBM;
+    if (u >= p.B * p.H * nk) return false;
+    const int bh = u / nk;
+    w.kt = u - bh * nk;
+    w.b = bh / p.H;
+    w.h = bh - w.b * p.H;
+    w.q_start = w.b * p.Sq;
+    w.Lq = p.Sq;
+    w.k_start = w.b * p.Sk;
+    w.Lk = p.Sk;
+    w.tile0 = w.b * ((p.Sq + kBN - 1) / kBN);
+  } else {
+    while (true) {
+      if (w.b >= p.B) return false;
+      if (u < w.base + w.units) break;
+      w.base += w.units;
+      w.b += 1;
+      bwd_load_seq(p, w, report);
+    }
+    const int rem = u - w.base;
+    const int nk = w.units / p.H;
+    w.h = rem / nk;
+    w.kt = rem - w.h * nk;
+  }
+  const int nq = (w.Lq + kBN - 1) / kBN;
   // causal (top-left): query tile i has a row >= every key of tile kt from i = kt on
   w.i0 = p.causal ? w.kt : 0;
   w.n = max(0, nq - w.i0);
@@ -210,6 +283,7 @@ __device__ __forceinline__ bool bwd_unit(const BwdParams& p, int k, BUnit& w) {
 }
 
 // Steps of this CTA in order, across its units (units without steps skipped).
+template <bool VARLEN>
 struct StepIter {
   int k;     // unit counter of this CTA
   BUnit w;
@@ -218,19 +292,20 @@ struct StepIter {
   __device__ __forceinline__ void start(const BwdParams& p) {
     k = 0;
     j = 0;
-    ok = bwd_unit(p, k, w);
-    while (ok && w.n == 0) ok = bwd_unit(p, ++k, w);
+    bwd_walk<VARLEN>(p, w, false);
+    ok = bwd_unit<VARLEN>(p, k, w);
+    while (ok && w.n == 0) ok = bwd_unit<VARLEN>(p, ++k, w);
   }
   __device__ __forceinline__ void next(const BwdParams& p) {
     if (++j < w.n) return;
     j = 0;
-    do ok = bwd_unit(p, ++k, w);
+    do ok = bwd_unit<VARLEN>(p, ++k, w);
     while (ok && w.n == 0);
   }
 };
 
 // ------------------------------------------------------------- P and dS
-template <int D, bool BF16>
+template <int D, bool BF16, bool VARLEN>
 __device__ void ds_role(const BwdParams& p, uint32_t tmem, uint8_t* base, uint32_t bars,
                         const Ctl& ctl) {
   using L = BLayout<D>;
@@ -245,17 +320,17 @@ __device__ void ds_role(const BwdParams& p, uint32_t tmem, uint8_t* base, uint32
   auto bar = [&](int i) { return bars + 8u * i; };
   const uint64_t c2 = ptx::f2(p.scale_log2, p.scale_log2);
 
-  StepIter cur;
+  StepIter<VARLEN> cur;
   cur.start(p);
   for (uint32_t g = 0; cur.ok; ++g) {
-    const BUnit w = cur.w;
+    const BUnit& w = cur.w;
     const int i = w.i0 + cur.j;
     const int key = w.kt * kBM + r;
     const int qb = i * kBN + 64 * half;
     // columns c (query qb + c) visible to this key: c >= cmin and qb + c < Sq
     const int cmin = p.causal ? key - qb : 0;
-    const int cmax = p.Sq - qb - 1;
-    const bool row_ok = key < p.Sk;
+    const int cmax = w.Lq - qb - 1;
+    const bool row_ok = key < w.Lk;
     const bool full = row_ok && cmin <= 0 && cmax >= 63;
 
     // ---- P^T = 2^(scale log2e (S^T - LSE / scale)), 16-bit, over S^T
@@ -328,7 +403,7 @@ __device__ void ds_role(const BwdParams& p, uint32_t tmem, uint8_t* base, uint32
 }
 
 // -------------------------------------------------- dQ and the dK/dV epilogue
-template <int D, bool BF16>
+template <int D, bool BF16, bool VARLEN>
 __device__ void dq_role(const BwdParams& p, uint32_t tmem, uint32_t smem, uint8_t* base,
                         uint32_t bars, const Ctl& ctl) {
   using L = BLayout<D>;
@@ -342,10 +417,11 @@ __device__ void dq_role(const BwdParams& p, uint32_t tmem, uint32_t smem, uint8_
   uint16_t* const DV = static_cast<uint16_t*>(p.dv);
   uint32_t g = 0, u_cnt = 0, stg_n = 0, stf_n = 0;
   BUnit w;
-  for (int k = 0; bwd_unit(p, k, w); ++k) {
+  bwd_walk<VARLEN>(p, w, false);
+  for (int k = 0; bwd_unit<VARLEN>(p, k, w); ++k) {
     const int key = w.kt * kBM + r;
-    const bool key_ok = key < p.Sk;
-    const long long krow = (static_cast<long long>(w.b) * p.Sk + key) * p.H + w.h;
+    const bool key_ok = key < w.Lk;
+    const long long krow = (static_cast<long long>(w.k_start) + key) * p.H + w.h;
     if (w.n == 0) {  // no query sees these keys: dK = dV = 0
       if (key_ok) {
         uint4* a = reinterpret_cast<uint4*>(DK + krow * D);
@@ -360,7 +436,9 @@ __device__ void dq_role(const BwdParams& p, uint32_t tmem, uint32_t smem, uint8_
       ptx::tc_fence_after();
       const uint32_t st = g & 1u;
       const bool issuer = threadIdx.x == kDqWarp0 * 32;
-      const int q0 = (w.i0 + j) * kBN, bh = w.b * p.H + w.h;
+      // the tile's first query row and the slice: dense [B*H, Sq, D], packed [H, Tq, D]
+      const int q0 = (VARLEN ? w.q_start : 0) + (w.i0 + j) * kBN;
+      const int slice = VARLEN ? w.h : w.b * p.H + w.h;
       auto stage_box = [&](int pos, const uint32_t (&v)[32]) {  // row r of a box, swizzled
         uint8_t* const row = base + L::dq_box_off(st, pos) + r * 128;
 #pragma unroll
@@ -375,8 +453,8 @@ __device__ void dq_role(const BwdParams& p, uint32_t tmem, uint32_t smem, uint8_
         ptx::mbar_arrive(bar(L::STG));
         if (issuer) {
           if (!wait_bar(bar(L::STG), stg_n & 1u, ctl)) return false;
-          tma_reduce_add_3d(&p.tm_dq, smem + L::dq_box_off(st, 0), x0, q0, bh);
-          tma_reduce_add_3d(&p.tm_dq, smem + L::dq_box_off(st, 1), x0 + 32, q0, bh);
+          tma_reduce_add_3d(&p.tm_dq, smem + L::dq_box_off(st, 0), x0, q0, slice);
+          tma_reduce_add_3d(&p.tm_dq, smem + L::dq_box_off(st, 1), x0 + 32, q0, slice);
           bulk_commit();
           bulk_wait_read();
         }
@@ -441,7 +519,7 @@ __device__ void dq_role(const BwdParams& p, uint32_t tmem, uint32_t smem, uint8_
 }
 
 // -------------------------------------------------------------------- MMA
-template <int D, bool BF16>
+template <int D, bool BF16, bool VARLEN>
 __device__ void mma_loop(const BwdParams& p, uint32_t smem, uint32_t tmem, uint32_t bars,
                          const Ctl& ctl) {
   using L = BLayout<D>;
@@ -479,7 +557,8 @@ __device__ void mma_loop(const BwdParams& p, uint32_t smem, uint32_t tmem, uint3
   // is in TMEM, S^T(g+1) (P(g) is consumed by dV(g) before it), then dK(g) and
   // dQ(g) = dS K into the dP^T columns once dS(g) is ready.
   BUnit w;
-  for (int k = 0; bwd_unit(p, k, w); ++k) {
+  bwd_walk<VARLEN>(p, w, false);
+  for (int k = 0; bwd_unit<VARLEN>(p, k, w); ++k) {
     if (w.n == 0) continue;
     if (!wait_bar(bar(L::KVF), kv_cnt & 1u, ctl)) return;
     ++kv_cnt;
@@ -536,17 +615,18 @@ __device__ void mma_loop(const BwdParams& p, uint32_t smem, uint32_t tmem, uint3
 }
 
 // ------------------------------------------------------------------- load
-template <int D>
+template <int D, bool VARLEN>
 __device__ void load_loop(const BwdParams& p, uint32_t smem, uint32_t bars, const Ctl& ctl,
                           uint32_t& g, uint32_t& kv_cnt) {
   using L = BLayout<D>;
   auto bar = [&](int i) { return bars + 8u * i; };
   BUnit w;
-  for (int k = 0; bwd_unit(p, k, w); ++k) {
+  bwd_walk<VARLEN>(p, w, true);
+  for (int k = 0; bwd_unit<VARLEN>(p, k, w, true); ++k) {
     if (w.n == 0) continue;
     if (kv_cnt > 0 && !wait_bar(bar(L::KVE), (kv_cnt - 1) & 1u, ctl)) return;
     ptx::mbar_arrive_expect_tx(bar(L::KVF), 2 * L::kTile);
-    const int krow = w.b * p.Sk + w.kt * kBM;
+    const int krow = w.k_start + w.kt * kBM;
 #pragma unroll
     for (int blk = 0; blk < D / 64; ++blk) {
       ptx::tma_load_3d(smem + L::kKOff + blk * L::kBlk, &p.tm_k, bar(L::KVF), blk * 64, w.h, krow);
@@ -555,9 +635,9 @@ __device__ void load_loop(const BwdParams& p, uint32_t smem, uint32_t bars, cons
     ++kv_cnt;
     for (int j = 0; j < w.n; ++j, ++g) {
       const uint32_t st = g & 1u;
-      const int qrow = w.b * p.Sq + (w.i0 + j) * kBN;
-      const int nq = (p.Sq + kBN - 1) / kBN;
-      const long long tile = (static_cast<long long>(w.b) * p.H + w.h) * nq + w.i0 + j;
+      const int qrow = w.q_start + (w.i0 + j) * kBN;
+      const long long tile = static_cast<long long>(w.tile0) * p.H +
+                             static_cast<long long>(w.h) * ((w.Lq + kBN - 1) / kBN) + w.i0 + j;
       // Q tile and S bias
       if (g >= 2 && !wait_bar(bar(L::QE0 + st), ((g >> 1) - 1) & 1u, ctl)) return;
       ptx::mbar_arrive_expect_tx(bar(L::QF0 + st), L::kTile + kBiasBytes);
@@ -580,7 +660,7 @@ __device__ void load_loop(const BwdParams& p, uint32_t smem, uint32_t bars, cons
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool VARLEN>
 __global__ void __maxnreg__(128) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
   using L = BLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -628,20 +708,20 @@ __global__ void __maxnreg__(128) attn_bwd_kernel(const __grid_constant__ BwdPara
   const Ctl ctl{abort_flag, p.err, p.timeout_ns};
 
   if (warp < kDsWarps) {
-    ds_role<D, BF16>(p, tmem, base, bars, ctl);
+    ds_role<D, BF16, VARLEN>(p, tmem, base, bars, ctl);
   } else if (warp < kMmaWarp) {
-    dq_role<D, BF16>(p, tmem, smem, base, bars, ctl);
+    dq_role<D, BF16, VARLEN>(p, tmem, smem, base, bars, ctl);
     if (threadIdx.x == kDqWarp0 * 32) bulk_wait_all();  // every reduce-add landed
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      mma_loop<D, BF16>(p, smem, tmem, bars, ctl);
+      mma_loop<D, BF16, VARLEN>(p, smem, tmem, bars, ctl);
       const uint32_t done = bars + 8u * L::DONE;
       ptx::mma_commit(done);
       wait_bar(done, 0, ctl, false);
     }
   } else if (lane == 0) {
     uint32_t g = 0, kv_cnt = 0;
-    load_loop<D>(p, smem, bars, ctl, g, kv_cnt);
+    load_loop<D, VARLEN>(p, smem, bars, ctl, g, kv_cnt);
     // no TMA write may land after the CTA exits
     if (kv_cnt > 0) wait_bar(bars + 8u * L::KVF, (kv_cnt - 1) & 1u, ctl, false);
     for (uint32_t st = 0; st < 2 && st < g; ++st) {
@@ -669,28 +749,19 @@ __device__ __forceinline__ void split3_bf16(float v, uint16_t (&out)[kBiasParts]
   }
 }
 
-// Per query row (b, h, q) of every query tile, q < Sq padded to whole tiles:
-// the bias operands of the two products, -LSE/scale (S^T) and -D with
-// D = sum_d dO * O (dP^T), each split in three bf16 parts at k = 0, 1, 2 of
-// the row (k = 3..15 zero); rows past Sq are all zero.  One warp per row.
+// One warp, one query row: row r of the bias tile t, the two per-query terms
+// -LSE/scale (S^T) and -D with D = sum_d dO * O (dP^T), each split in three
+// bf16 parts at k = 0, 1, 2 of the row (k = 3..15 zero).  orow < 0: a padding
+// row past the sequence, all zero.  A row without keys (LSE = -inf) is seen by
+// no work unit; its terms are written as zero.
 template <int D, bool BF16>
-__global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const uint16_t* __restrict__ o,
-                                                           const uint16_t* __restrict__ dout,
-                                                           const float* __restrict__ lse,
-                                                           uint8_t* __restrict__ bias, int B,
-                                                           int H, int Sq, float scale) {
-  const int nq = (Sq + kBN - 1) / kBN;
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (row >= static_cast<long long>(B) * H * nq * kBN) return;  // row = (b*H + h) * nq*128 + q
+__device__ __forceinline__ void bias_row(const uint16_t* __restrict__ o,
+                                         const uint16_t* __restrict__ dout, long long orow,
+                                         const float* lse_elem, float scale, uint8_t* t, int r) {
   const int lane = threadIdx.x & 31;
-  const int q = static_cast<int>(row % (static_cast<long long>(nq) * kBN));
-  const long long bh = row / (static_cast<long long>(nq) * kBN);
-  const int h = static_cast<int>(bh % H);
-  const int b = static_cast<int>(bh / H);
   float dsum = 0.0f, nls = 0.0f;
-  if (q < Sq) {
+  if (orow >= 0) {
     constexpr int PER = D / 32;  // 2 or 4 elements per lane
-    const long long orow = (static_cast<long long>(b) * Sq + q) * H + h;
     const uint16_t* a = o + orow * D + lane * PER;
     const uint16_t* c = dout + orow * D + lane * PER;
 #pragma unroll
@@ -702,14 +773,13 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const uint16_t* __res
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
-    nls = -lse[bh * Sq + q] / scale;
+    const float l = *lse_elem;
+    nls = isfinite(l) ? -l / scale : 0.0f;
   }
   if (lane == 0) {
-    uint8_t* const t = bias + (bh * nq + q / kBN) * 2 * kBiasBytes;
-    const int r = q % kBN;
     uint16_t sp[kBiasParts], dp[kBiasParts];
-    split3_bf16(q < Sq ? nls : 0.0f, sp);
-    split3_bf16(q < Sq ? -dsum : 0.0f, dp);
+    split3_bf16(nls, sp);
+    split3_bf16(-dsum, dp);
     *reinterpret_cast<uint4*>(t + bias_offset(r, 0)) =
         make_uint4(sp[0] | (static_cast<uint32_t>(sp[1]) << 16), sp[2], 0u, 0u);
     *reinterpret_cast<uint4*>(t + bias_offset(r, 8)) = make_uint4(0u, 0u, 0u, 0u);
@@ -719,7 +789,113 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const uint16_t* __res
   }
 }
 
-// dQ[b, q, h, :] = scale * acc[b, h, q, :] in the input dtype.
+// Dense sequences: every row (b, h, q) of every query tile, q < Sq padded to
+// whole tiles; tile (b * H + h) * nq + q / 128.  One warp per row.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const uint16_t* __restrict__ o,
+                                                           const uint16_t* __restrict__ dout,
+                                                           const float* __restrict__ lse,
+                                                           uint8_t* __restrict__ bias, int B,
+                                                           int H, int Sq, float scale) {
+  const int nq = (Sq + kBN - 1) / kBN;
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (row >= static_cast<long long>(B) * H * nq * kBN) return;  // row = (b*H + h) * nq*128 + q
+  const int q = static_cast<int>(row % (static_cast<long long>(nq) * kBN));
+  const long long bh = row / (static_cast<long long>(nq) * kBN);
+  const int h = static_cast<int>(bh % H);
+  const int b = static_cast<int>(bh / H);
+  const bool real = q < Sq;
+  bias_row<D, BF16>(o, dout, real ? (static_cast<long long>(b) * Sq + q) * H + h : -1,
+                    real ? lse + bh * Sq + q : nullptr, scale,
+                    bias + (bh * nq + q / kBN) * 2 * kBiasBytes, q % kBN);
+}
+
+// Packed sequences, one block of 1024 threads: tiles[b] = the 128-query tiles
+// of sequences 0 .. b-1 (b = 0..B) and tiles[B + 1] = 1 when every sequence's
+// bounds are well formed (0 <= cu_q[b] <= cu_q[b+1] <= Sq, the same for cu_k),
+// else 0 and the error word reports ATTN_ERR_BAD_SEQLENS.  Well-formed bounds
+// tile at most Sq rows, so tiles[B] <= (Sq + 127 B) / 128.
+static __global__ void __launch_bounds__(1024)
+    attn_bwd_tiles_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k,
+                          int B, int Sq, int Sk, int32_t* __restrict__ tiles, int* err) {
+  __shared__ int part[1024];
+  __shared__ int bad;
+  const int t = threadIdx.x;
+  if (t == 0) bad = 0;
+  __syncthreads();
+  auto count = [&](int b, bool& ok) {
+    const int q0 = __ldg(cu_q + b), q1 = __ldg(cu_q + b + 1);
+    const int k0 = __ldg(cu_k + b), k1 = __ldg(cu_k + b + 1);
+    ok = 0 <= q0 && q0 <= q1 && q1 <= Sq && 0 <= k0 && k0 <= k1 && k1 <= Sk;
+    return ok ? (q1 - q0 + kBN - 1) / kBN : 0;
+  };
+  const int per = (B + 1023) / 1024;
+  const int b0 = min(B, t * per), b1 = min(B, b0 + per);
+  int sum = 0;
+  bool any_bad = false;
+  for (int b = b0; b < b1; ++b) {
+    bool ok;
+    sum += count(b, ok);
+    any_bad |= !ok;
+  }
+  if (any_bad) atomicOr(&bad, 1);
+  part[t] = sum;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {  // inclusive scan of part[]
+    const int v = t >= off ? part[t - off] : 0;
+    __syncthreads();
+    part[t] += v;
+    __syncthreads();
+  }
+  int run = part[t] - sum;
+  for (int b = b0; b < b1; ++b) {
+    tiles[b] = run;
+    bool ok;
+    run += count(b, ok);
+  }
+  if (t == 1023) {
+    tiles[B] = part[1023];
+    tiles[B + 1] = bad ? 0 : 1;
+    if (bad) atomicOr(err, kErrBadSeqlens);
+  }
+}
+
+// Packed sequences: every row of every query tile (tiles[B] * H tiles of 128
+// rows); tile t = tiles[b] * H + h * nq(b) + i belongs to the largest b with
+// tiles[b] * H <= t.  Rows past the sequence are zero.  One warp per row;
+// nothing when the bounds were malformed.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) attn_bwd_pre_varlen_kernel(
+    const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+    const float* __restrict__ lse, uint8_t* __restrict__ bias, const int32_t* __restrict__ tiles,
+    const int32_t* __restrict__ cu_q, int B, int H, int Tq, float scale) {
+  if (__ldg(tiles + B + 1) == 0) return;
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (row >= static_cast<long long>(__ldg(tiles + B)) * H * kBN) return;
+  const long long t = row / kBN;
+  const int r = static_cast<int>(row - t * kBN);
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<long long>(__ldg(tiles + mid)) * H <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  const int tb = __ldg(tiles + lo);
+  const int nq = __ldg(tiles + lo + 1) - tb;  // > 0: tile t lies in sequence lo's range
+  const long long rem = t - static_cast<long long>(tb) * H;
+  const int h = static_cast<int>(rem / nq);
+  const int i = static_cast<int>(rem - static_cast<long long>(h) * nq);
+  const int q0 = __ldg(cu_q + lo), lq = __ldg(cu_q + lo + 1) - q0;
+  const int pos = i * kBN + r;
+  const bool real = pos < lq;
+  const long long q = static_cast<long long>(q0) + pos;
+  bias_row<D, BF16>(o, dout, real ? q * H + h : -1,
+                    real ? lse + static_cast<long long>(h) * Tq + q : nullptr, scale,
+                    bias + t * 2 * kBiasBytes, r);
+}
+
+// dQ[b, q, h, :] = scale * acc[b, h, q, :] in the input dtype; packed
+// sequences are one batch of Tq rows (B = 1, Sq = Tq; rows of no sequence: 0).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const float* __restrict__ acc,
                                                             uint16_t* __restrict__ dq, int B,
@@ -728,7 +904,7 @@ __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const float* __restr
   const long long n = static_cast<long long>(B) * H * Sq * (D / 2);
   if (i >= n) return;
   const int d2 = static_cast<int>(i % (D / 2));
-  const long long row = i / (D / 2);  // (b * H + h) * Sq + q
+  const long long row = i / (D / 2);  // dense (b * H + h) * Sq + q; packed h * Sq + q
   const int q = static_cast<int>(row % Sq);
   const long long bh = row / Sq;
   const int h = static_cast<int>(bh % H);
@@ -739,20 +915,32 @@ __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const float* __restr
       pk;
 }
 
+// The four launches of one backward.  Dense: bias holds B*H*nq tiles.  Packed
+// (p.varlen): bias holds tiles_bound*H tiles, p.tiles B + 2 ints, and the
+// accumulator is [H, Tq, D] (Tq = p.Sq rows).
 template <int D, bool BF16>
 cudaError_t launch_bwd(const BwdParams& p, const uint16_t* o, const uint16_t* dout,
-                       const float* lse, uint8_t* bias, uint16_t* dq, int grid,
-                       cudaStream_t stream) {
-  const long long rows = static_cast<long long>(p.B) * p.Sq * p.H;
+                       const float* lse, uint8_t* bias, int32_t* tiles, long long tiles_bound,
+                       uint16_t* dq, int grid, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.Tq) * p.H;
   cudaError_t e = cudaMemsetAsync(p.dq_acc, 0, static_cast<size_t>(rows) * D * sizeof(float),
                                   stream);
   if (e != cudaSuccess) return e;
-  const long long prow = static_cast<long long>(p.B) * p.H * ((p.Sq + kBN - 1) / kBN) * kBN;
-  attn_bwd_pre_kernel<D, BF16><<<static_cast<unsigned>((prow + 7) / 8), 256, 0, stream>>>(
-      o, dout, lse, bias, p.B, p.H, p.Sq, p.scale);
+  if (p.varlen) {
+    attn_bwd_tiles_kernel<<<1, 1024, 0, stream>>>(p.cu_q, p.cu_k, p.B, p.Sq, p.Sk, tiles, p.err);
+    const long long prow = tiles_bound * p.H * kBN;
+    attn_bwd_pre_varlen_kernel<D, BF16><<<static_cast<unsigned>((prow + 7) / 8), 256, 0, stream>>>(
+        o, dout, lse, bias, tiles, p.cu_q, p.B, p.H, p.Tq, p.scale);
+  } else {
+    const long long prow = static_cast<long long>(p.B) * p.H * ((p.Sq + kBN - 1) / kBN) * kBN;
+    attn_bwd_pre_kernel<D, BF16><<<static_cast<unsigned>((prow + 7) / 8), 256, 0, stream>>>(
+        o, dout, lse, bias, p.B, p.H, p.Sq, p.scale);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const void* fn = reinterpret_cast<const void*>(&attn_bwd_kernel<D, BF16>);
+  // packed sequences walk their bounds; the dense instantiation has no walk
+  const void* fn = p.varlen ? reinterpret_cast<const void*>(&attn_bwd_kernel<D, BF16, true>)
+                            : reinterpret_cast<const void*>(&attn_bwd_kernel<D, BF16, false>);
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, BLayout<D>::kAlloc);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<BwdParams*>(&p)};
@@ -760,7 +948,7 @@ cudaError_t launch_bwd(const BwdParams& p, const uint16_t* o, const uint16_t* do
   if (e != cudaSuccess) return e;
   const long long pairs = rows * (D / 2);
   attn_bwd_post_kernel<D, BF16><<<static_cast<unsigned>((pairs + 255) / 256), 256, 0, stream>>>(
-      p.dq_acc, dq, p.B, p.H, p.Sq, p.scale);
+      p.dq_acc, dq, p.varlen ? 1 : p.B, p.H, p.varlen ? p.Tq : p.Sq, p.scale);
   return cudaGetLastError();
 }
 

@@ -149,19 +149,30 @@ def test_window_entry_point_shares_attn_fwd_checks(lib):
 
 def test_bwd_rejects_zero_scale_and_bad_sizes(lib):
     a = dict(q=A, k=A + 0x100, v=A + 0x200, o=A + 0x300, do=A + 0x400, lse=A + 0x500,
-             dq=A + 0x600, dk=A + 0x700, dv=A + 0x800, ws=A + 0x1000)
-    def bwd(scale=0.125, D=64, Sq=128, Sk=128, dtype=0, ws_bytes=1 << 30, **kw):
+             dq=A + 0x600, dk=A + 0x700, dv=A + 0x800, ws=A + 0x1000, cq=None, ck=None)
+    def bwd(scale=0.125, D=64, B=1, Sq=128, Sk=128, dtype=0, ws_bytes=1 << 30, **kw):
         x = dict(a, **kw)
         return lib.attn_bwd(x["q"], x["k"], x["v"], x["o"], x["do"], x["lse"], x["dq"], x["dk"],
-                            x["dv"], 1, 2, Sq, Sk, D, ctypes.c_float(scale), 1, x["ws"], ws_bytes,
-                            dtype, None)
+                            x["dv"], B, 2, Sq, Sk, D, ctypes.c_float(scale), 1, x["cq"], x["ck"],
+                            x["ws"], ws_bytes, dtype, None)
     assert bwd(scale=0.0) == pkg.ATTN_ERR_UNSUPPORTED
     assert bwd(scale=float("nan")) == pkg.ATTN_ERR_INVALID_ARG
     assert bwd(D=96) == pkg.ATTN_ERR_UNSUPPORTED
     assert bwd(Sk=0) == pkg.ATTN_ERR_INVALID_ARG
     assert bwd(ws=A + 0x1010) == pkg.ATTN_ERR_MISALIGNED
     assert bwd(ws_bytes=16) == pkg.ATTN_ERR_INVALID_ARG
-    assert bwd(Sq=0) == pkg.ATTN_OK
+    assert bwd(B=0) == pkg.ATTN_OK
+    # packed sequences: both bounds arrays or neither, 4-byte aligned
+    assert bwd(cq=A + 0x900) == pkg.ATTN_ERR_INVALID_ARG
+    assert bwd(ck=A + 0x900) == pkg.ATTN_ERR_INVALID_ARG
+    assert bwd(cq=A + 0x902, ck=A + 0x980) == pkg.ATTN_ERR_MISALIGNED
+    assert bwd(cq=A + 0x900, ck=A + 0x980, ws_bytes=16) == pkg.ATTN_ERR_INVALID_ARG
     n = ctypes.c_size_t(0)
-    assert lib.attn_bwd_workspace(1, 2, 300, 128, ctypes.byref(n)) == pkg.ATTN_OK
+    assert lib.attn_bwd_workspace(1, 2, 300, 128, 0, ctypes.byref(n)) == pkg.ATTN_OK
+    # dense: fp32 accumulator + 8 KiB per 128-query tile and head
     assert n.value == ((2 * 300 * 128 * 4 + 255) // 256) * 256 + 2 * 3 * 8192
+    # packed, 5 sequences over 300 rows: at most (300 + 127 * 5) // 128 = 7 tiles per head,
+    # plus 4 * (5 + 2) bytes of tile offsets rounded up to 256
+    assert lib.attn_bwd_workspace(5, 2, 300, 128, 1, ctypes.byref(n)) == pkg.ATTN_OK
+    assert n.value == ((2 * 300 * 128 * 4 + 255) // 256) * 256 + 2 * 7 * 8192 + 256
+    assert lib.attn_bwd_workspace(1, 2, 300, 96, 0, ctypes.byref(n)) == pkg.ATTN_ERR_UNSUPPORTED

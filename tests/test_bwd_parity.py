@@ -28,7 +28,7 @@ import pytest
 import torch
 
 import scaled_dot_product_tcgen05_gb300 as pkg
-from oracle.sdpa_oracle import attention_backward_dense
+from oracle.sdpa_oracle import attention_backward_dense, attention_backward_varlen
 
 pytestmark = pytest.mark.gpu
 
@@ -54,7 +54,8 @@ def _case(seed, B, H, Sq, Sk, D, dt):
 def compare_grads(got, ref, what):
     stats = {}
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
-        gg = g.float().cpu().numpy().astype(np.float64)
+        with np.errstate(invalid="ignore"):  # unwritten rows (keys of no sequence) may be NaN
+            gg = g.float().cpu().numpy().astype(np.float64)
         sel = ~np.isnan(r)
         assert np.all(np.isfinite(gg[sel])), f"{what}: non-finite {name}"
         rms = max(float(np.sqrt(np.mean(r[sel] ** 2))), 1e-30)
@@ -126,3 +127,98 @@ def test_bwd_dk_dv_deterministic():
     b = _run(q, k, v, do, True, 0.09)
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
     assert torch.allclose(a[0].float(), b[0].float(), atol=1e-2, rtol=0)
+
+
+# ------------------------------------------------------------ packed sequences
+def _packed_case(seed, lens_q, lens_k, H, D, dt, lead=0, tail=0):
+    """Packed batch with ``lead`` rows before and ``tail`` rows after the sequences
+    (rows of no sequence, finite values)."""
+    g = torch.Generator().manual_seed(seed)
+    cq = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32) + lead
+    ck = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32) + lead
+    Tq, Tk = int(cq[-1]) + tail, int(ck[-1]) + tail
+    mk = lambda T: torch.randn(T, H, D, generator=g).to(dt)  # noqa: E731
+    return mk(Tq), mk(Tk), mk(Tk), mk(Tq), cq, ck
+
+
+def _run_packed(q, k, v, do, cq, ck, causal, scale, poison_outside=True):
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    cqd, ckd = (torch.from_numpy(c).to(DEV) for c in (cq, ck))
+    o, lse = pkg.attn_fwd(qd, kd, vd, causal=causal, scale=scale, cu_seqlens_q=cqd,
+                          cu_seqlens_k=ckd)
+    if poison_outside:  # the forward leaves these rows unwritten: anything may be there
+        for sl in (slice(0, int(cq[0])), slice(int(cq[-1]), q.shape[0])):
+            o[sl] = float("nan")
+            lse[:, sl] = float("nan")
+    dq, dk, dv = pkg.attn_bwd(qd, kd, vd, o, dod, lse, causal=causal, scale=scale,
+                              cu_seqlens_q=cqd, cu_seqlens_k=ckd)
+    st = pkg.attn_check()
+    assert st == pkg.ATTN_OK, pkg.status_string(st)
+    return dq, dk, dv
+
+
+VARLEN_CASES = [
+    # (lens_q, lens_k, H, D, dtype, causal, lead, tail)
+    ([300, 0, 129, 1, 700], [300, 50, 129, 1, 700], 2, 128, BF, True, 0, 0),
+    ([200, 513, 64], [333, 100, 64], 2, 64, FP, False, 0, 0),
+    ([128, 256], [128, 256], 2, 128, BF, True, 0, 0),
+    ([37, 90, 200], [37, 0, 150], 2, 128, BF, True, 0, 0),      # a sequence without keys
+    ([150, 300], [170, 260], 2, 64, BF, True, 20, 33),         # rows of no sequence
+    ([1000, 3, 517], [1000, 400, 517], 1, 128, FP, False, 5, 0),
+]
+
+
+def _vid(c):
+    return "q{}k{}H{}D{}{}{}l{}t{}".format("-".join(map(str, c[0])), "-".join(map(str, c[1])),
+                                          c[2], c[3], "bf" if c[4] == BF else "fp",
+                                          "c" if c[5] else "", c[6], c[7])
+
+
+@pytest.mark.parametrize("case", VARLEN_CASES, ids=_vid)
+def test_bwd_varlen_parity(case):
+    lens_q, lens_k, H, D, dt, causal, lead, tail = case
+    q, k, v, do, cq, ck = _packed_case(sum(lens_q) + 7 * sum(lens_k), lens_q, lens_k, H, D, dt,
+                                       lead, tail)
+    scale = 1.0 / math.sqrt(D)
+    got = _run_packed(q, k, v, do, cq, ck, causal, scale)
+    ref = attention_backward_varlen(q, k, v, do, cq, ck, scale, causal)
+    compare_grads(got, ref, _vid(case))
+    dq = got[0].float().cpu()
+    assert torch.all(dq[:int(cq[0])] == 0) and torch.all(dq[int(cq[-1]):] == 0)
+    for b in range(len(lens_q)):  # keys no query sees: exactly zero
+        k0, k1 = int(ck[b]), int(ck[b + 1])
+        unseen = k0 + (min(lens_q[b], lens_k[b]) if causal else (lens_k[b] if lens_q[b] else 0))
+        if unseen < k1:
+            assert torch.all(got[1][unseen:k1] == 0) and torch.all(got[2][unseen:k1] == 0)
+
+
+def test_bwd_varlen_equal_lengths_match_dense():
+    """Sequences of one length packed back to back, with the same O and LSE, give the
+    dense call's dK, dV bit for bit (dQ's fp32 reduce-adds may land in another order)."""
+    B, S, H, D = 3, 333, 2, 128
+    q, k, v, do = (t.to(DEV) for t in _case(91, B, H, S, S, D, BF))
+    scale = 1.0 / math.sqrt(D)
+    o, lse = pkg.attn_fwd(q, k, v, causal=True, scale=scale)
+    dense = pkg.attn_bwd(q, k, v, o, do, lse, causal=True, scale=scale)
+    cu = torch.arange(0, (B + 1) * S, S, dtype=torch.int32, device=DEV)
+    flat = lambda t: t.reshape(B * S, H, D)  # noqa: E731
+    packed = pkg.attn_bwd(flat(q), flat(k), flat(v), flat(o), flat(do),
+                          lse.permute(1, 0, 2).reshape(H, B * S).contiguous(), causal=True,
+                          scale=scale, cu_seqlens_q=cu, cu_seqlens_k=cu)
+    st = pkg.attn_check()
+    assert st == pkg.ATTN_OK, pkg.status_string(st)
+    assert torch.equal(flat(dense[1]), packed[1]) and torch.equal(flat(dense[2]), packed[2])
+    assert torch.allclose(flat(dense[0]).float(), packed[0].float(), atol=1e-2, rtol=0)
+
+
+def test_bwd_varlen_malformed_bounds_are_reported():
+    """Decreasing sequence bounds: the call does no work and attn_check reports them."""
+    q, k, v, do, cq, ck = _packed_case(5, [200, 100], [200, 100], 2, 128, BF)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    good_q, good_k = (torch.from_numpy(c).to(DEV) for c in (cq, ck))
+    o, lse = pkg.attn_fwd(qd, kd, vd, causal=True, cu_seqlens_q=good_q, cu_seqlens_k=good_k)
+    assert pkg.attn_check() == pkg.ATTN_OK
+    bad_q = torch.tensor([0, 250, 200], dtype=torch.int32, device=DEV)
+    pkg.attn_bwd(qd, kd, vd, o, dod, lse, causal=True, cu_seqlens_q=bad_q, cu_seqlens_k=good_k)
+    assert pkg.attn_check() == pkg.ATTN_ERR_BAD_SEQLENS
+    assert pkg.attn_check() == pkg.ATTN_OK  # the error word was cleared
