@@ -117,6 +117,20 @@ __device__ __forceinline__ bool decode_pair(const FwdParams& p, int k, Cursor& c
 }
 
 // ---------------------------------------------------------------- softmax
+// x rounded to the 16-bit input type (nearest even) and back to fp32.
+template <bool BF16>
+__device__ __forceinline__ float round16(float x) {
+  const uint32_t pk = ptx::pack2<BF16>(x, 0.0f);  // x in the low half
+  float y;
+  if constexpr (BF16) {
+    y = __uint_as_float(pk << 16);
+  } else {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}"
+        : "=f"(y) : "r"(pk));
+  }
+  return y;
+}
+
 // One K/V step of the online softmax for half of a query row: this thread owns
 // keys [64h, 64h+64) of S (the other half sits with the thread of the same lane
 // in warp w ^ 4, on the same SM sub-partition and TMEM lane quarter).  The two
@@ -154,7 +168,8 @@ __device__ __forceinline__ bool softmax_half_step(uint32_t tS, uint32_t tP, uint
     mx2 = ptx::max3(mx2, __uint_as_float(r[c + 4]), __uint_as_float(r[c + 5]));
     mx3 = ptx::max3(mx3, __uint_as_float(r[c + 6]), __uint_as_float(r[c + 7]));
   }
-  const float m_part = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cle;
+  const float r_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));  // this half's largest score
+  const float m_part = r_max * cle;
   *x_mine = m_part;
   // Both halves have read their S columns (tcgen05.ld waited) before either
   // overwrites the first 64 columns of the buffer with P.
@@ -171,7 +186,6 @@ __device__ __forceinline__ bool softmax_half_step(uint32_t tS, uint32_t tP, uint
 
   const float nm = -m_safe;
   float la = 0.f, lb = 0.f, lc = 0.f, ld = 0.f;
-  float lp0 = 0.f, lp1 = 0.f, lp2 = 0.f, lp3 = 0.f;
   uint32_t pk[32];
 #pragma unroll
   for (int c = 0; c < 64; c += 4) {
@@ -186,15 +200,17 @@ __device__ __forceinline__ bool softmax_half_step(uint32_t tS, uint32_t tP, uint
     ld += p3;
     pk[c / 2] = ptx::pack2<BF16>(p0, p1);
     pk[c / 2 + 1] = ptx::pack2<BF16>(p2, p3);
-    // the denominator sums the same 16-bit values the P.V product sees
-    lp0 = ptx::add_lo16<BF16>(lp0, pk[c / 2]);
-    lp1 = ptx::add_hi16<BF16>(lp1, pk[c / 2]);
-    lp2 = ptx::add_lo16<BF16>(lp2, pk[c / 2 + 1]);
-    lp3 = ptx::add_hi16<BF16>(lp3, pk[c / 2 + 1]);
   }
   ptx::tmem_st_x32(tP, pk);
-  st.l_x = st.l_x * alpha + ((la + lb) + (lc + ld));
-  st.l_p = st.l_p * alpha + ((lp0 + lp1) + (lp2 + lp3));
+  // O is normalised by the exact sum plus the rounding error of this half's
+  // largest value (computed exactly as in the loop, so the correction cancels
+  // that value's rounding in P.V): the largest values are the ones whose
+  // rounding would otherwise show in a peaked row, and the per-element loop
+  // keeps a single sum.
+  const float p_big = ptx::ex2(fmaf(r_max, cle, nm));
+  const float sum = (la + lb) + (lc + ld);
+  st.l_x = st.l_x * alpha + sum;
+  st.l_p = st.l_p * alpha + (sum + (round16<BF16>(p_big) - p_big));
 
   if (!first && __any_sync(0xffffffffu, rescale)) {
     if (!wait_bar_warp(pvd_bar, pvd_parity, ctl)) return false;

@@ -45,6 +45,22 @@ def test_workload_parity(name):
     compare(o, lse, o_ref, l_ref, what=name)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_peaked_head_dim_128(dtype, causal):
+    """The peaked draw (Q, K ~ N(0, 16)) at head dim 128, the CTA-pair kernel's case.
+
+    Nearly one-hot rows are where the rounding of P to 16 bits shows in O unless
+    the softmax denominator accounts for it; 24 heads of 2048 x 2048.
+    """
+    wl = W.Workload(name="peaked_d128", wid=3, B=2, H=12, Sq=2048, Sk=2048, D=128, dtype=dtype,
+                    causal=causal, std=(4.0, 4.0, 1.0), draw=3)
+    inp = W.make_inputs(wl)
+    o, lse = run_gpu(inp["q"], inp["k"], inp["v"], causal, wl.scale)
+    o_ref, l_ref = attention_dense(inp["q"], inp["k"], inp["v"], wl.scale, causal)
+    compare(o, lse, o_ref, l_ref, what=f"peaked_d128_{dtype}_{causal}")
+
+
 @pytest.mark.parametrize("name", ["long64k_causal", "long128k_causal"])
 def test_long_context_sampled_rows(name):
     """Full GPU run; the oracle checks 256 seeded rows on 4 seeded heads."""
