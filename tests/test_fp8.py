@@ -59,6 +59,7 @@ def _compare(o, lse, o_ref, l_ref, what):
     d = np.abs(og - o_ref)
     dl = np.abs(lg - l_ref) / np.maximum(1.0, np.abs(l_ref))
     stats = dict(o_max=float(d.max()), o_mean=float(d.mean()), lse=float(dl.max()))
+    print(f"{what}: {stats}")
     assert stats["o_max"] <= O_MAX and stats["o_mean"] <= O_MEAN and stats["lse"] <= LSE_REL, \
         f"{what}: {stats}"
     return stats
