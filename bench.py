@@ -489,22 +489,32 @@ def main(argv=None):
             dq_t, dk_t, dv_t = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     torch.cuda.synchronize()
 
-    def step():
+    # one set of device buffers; the end-to-end leg uses a second one as well
+    bs0 = dict(q=q, k=k, v=v, o=o, lse=lse)
+    if wl.backward:
+        bs0.update(dout=dout, dq=dq_t, dk=dk_t, dv=dv_t)
+
+    def run_step(bs):
         if wl.fp8:
-            pkg.attn_fwd_fp8(q, k, v, q_scale=qs, k_scale=ks, v_scale=vs, causal=wl.causal,
-                             scale=wl.scale, workspace=ws_fp8, out=o, lse=lse, stream=stream)
+            pkg.attn_fwd_fp8(bs["q"], bs["k"], bs["v"], q_scale=qs, k_scale=ks, v_scale=vs,
+                             causal=wl.causal, scale=wl.scale, workspace=ws_fp8, out=bs["o"],
+                             lse=bs["lse"], stream=stream)
             return
         if wl.backward:
-            pkg.attn_bwd(q, k, v, o, dout, lse, causal=wl.causal, scale=wl.scale,
-                         workspace=ws_bwd, dq=dq_t, dk=dk_t, dv=dv_t, stream=stream)
+            pkg.attn_bwd(bs["q"], bs["k"], bs["v"], bs["o"], bs["dout"], bs["lse"],
+                         causal=wl.causal, scale=wl.scale, workspace=ws_bwd, dq=bs["dq"],
+                         dk=bs["dk"], dv=bs["dv"], stream=stream)
             return
         if wl.decode:
-            pkg.attn_decode(q, k, v, causal=wl.causal, scale=wl.scale, workspace=ws_dec, out=o,
-                            lse=lse, stream=stream)
+            pkg.attn_decode(bs["q"], bs["k"], bs["v"], causal=wl.causal, scale=wl.scale,
+                            workspace=ws_dec, out=bs["o"], lse=bs["lse"], stream=stream)
             return
-        pkg.attn_fwd(q, k, v, causal=wl.causal, scale=wl.scale, cu_seqlens_q=cu,
-                     cu_seqlens_k=cu, out=o, lse=lse, window=wl.window, global_q=wl.global_q,
-                     stream=stream)
+        pkg.attn_fwd(bs["q"], bs["k"], bs["v"], causal=wl.causal, scale=wl.scale,
+                     cu_seqlens_q=cu, cu_seqlens_k=cu, out=bs["o"], lse=bs["lse"],
+                     window=wl.window, global_q=wl.global_q, stream=stream)
+
+    def step():
+        run_step(bs0)
 
     # ---- kernel-only timed region (inputs resident in HBM)
     for _ in range(args.warmup):
@@ -549,32 +559,53 @@ def main(argv=None):
         torch.cuda.synchronize()
         g_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq_t, dk_t, dv_t)]
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            q.copy_(q_h, non_blocking=True)
-            k.copy_(k_h, non_blocking=True)
-            v.copy_(v_h, non_blocking=True)
-            if wl.backward:
-                o.copy_(o_h, non_blocking=True)
-                lse.copy_(lse_h, non_blocking=True)
-                dout.copy_(do_h, non_blocking=True)
-                step()
-                for hbuf, dbuf in zip(g_h, (dq_t, dk_t, dv_t)):
-                    hbuf.copy_(dbuf, non_blocking=True)
-                return
-            step()
-            o_h.copy_(o, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
+    # Double-buffered: step i uploads its inputs into buffer set i % 2 on one
+    # copy stream while step i - 1 computes, and downloads its results on
+    # another; a set is refilled only after its previous results have left.
+    with torch.cuda.stream(stream):
+        bs1 = {name: torch.empty_like(t) for name, t in bs0.items()}
+    torch.cuda.synchronize()
+    sets = (bs0, bs1)
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    host_in = [("q", q_h), ("k", k_h), ("v", v_h)]
+    if wl.backward:  # inputs q, k, v, o, dO, LSE in; dQ, dK, dV out
+        host_in += [("o", o_h), ("lse", lse_h), ("dout", do_h)]
+        host_out = list(zip(g_h, ("dq", "dk", "dv")))
+    else:
+        host_out = [(o_h, "o"), (lse_h, "lse")]
+    freed = [None, None]
 
-    for _ in range(args.warmup):
-        e2e_step()
+    def e2e_steps(n):
+        for i in range(n):
+            bs = sets[i % 2]
+            if freed[i % 2] is not None:
+                up.wait_event(freed[i % 2])
+            with torch.cuda.stream(up):
+                for name, h in host_in:
+                    bs[name].copy_(h, non_blocking=True)
+            ready = torch.cuda.Event()
+            ready.record(up)
+            stream.wait_event(ready)
+            run_step(bs)
+            done = torch.cuda.Event()
+            done.record(stream)
+            down.wait_event(done)
+            with torch.cuda.stream(down):
+                for h, name in host_out:
+                    h.copy_(bs[name], non_blocking=True)
+            freed[i % 2] = torch.cuda.Event()
+            freed[i % 2].record(down)
+
+    e2e_steps(args.warmup)
+    torch.cuda.synchronize()
     e_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     barrier()
     torch.cuda.synchronize()
-    e_ev[0].record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e_ev[1].record(stream)
+    freed = [None, None]
+    e_ev[0].record(up)
+    e2e_steps(args.steps)
+    down.wait_event(freed[(args.steps - 1) % 2])
+    e_ev[1].record(down)
     torch.cuda.synchronize()
     barrier()
     e2e_ms = max_over_ranks(e_ev[0].elapsed_time(e_ev[1]) / args.steps, dev)
@@ -629,7 +660,9 @@ def main(argv=None):
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                      "kernel": kern, "kernel_ms": kernel_ms},
         "e2e": {"value": per_step / (e2e_ms * 1e-3), "unit": unit,
-                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "overlap": "double-buffered: step i+1's upload and step i-1's download run "
+                           "on two copy streams while step i computes"},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
         "cpu_baseline": cpu,
