@@ -246,6 +246,14 @@ int attn_fwd_fp8_workspace(int B, int H, int Sk, int D, size_t* bytes);
  * attn_check -- synchronise `stream`, then report and clear the device error
  * word of the current device: ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT,
  * ATTN_ERR_BAD_SEQLENS, or ATTN_ERR_CUDA if the stream itself failed.
+ *
+ * Debug environment (read at every call): ATTN_WAIT_TIMEOUT_MS bounds every
+ * device-side wait (default 5000); when one runs out the kernel sets the
+ * error word, its roles drain and it exits, leaving the context usable.
+ * ATTN_INJECT_FAULT (tests only, attn_fwd_decode): 1 = the first tile fill of
+ * block 0 is skipped, so that a wait runs out (ATTN_ERR_DEVICE_TIMEOUT from
+ * attn_check); 2 = the kernel is launched with an empty grid, which the
+ * launch rejects (the call returns ATTN_ERR_CUDA).
  */
 int attn_check(void* stream);
 

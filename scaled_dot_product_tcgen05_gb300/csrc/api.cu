@@ -40,6 +40,15 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 thread_local int t_last_grid = -1;
 thread_local int t_last_smem = -1;
 
+// Fault injection for the failure-detection tests, in attn_fwd_decode only:
+// ATTN_INJECT_FAULT=1 makes the decode kernel's block 0 skip its first fill,
+// so a bounded wait runs out; =2 launches an empty grid, which the launch
+// rejects.  Unset in normal use.
+int inject_from_env() {
+  const char* s = std::getenv("ATTN_INJECT_FAULT");
+  return s ? std::atoi(s) : 0;
+}
+
 long long timeout_ns_from_env() {
   const char* s = std::getenv("ATTN_WAIT_TIMEOUT_MS");
   long long ms = s ? std::atoll(s) : 0;
@@ -387,8 +396,10 @@ extern "C" int attn_fwd_decode(const void* q, const void* k_cache, const void* v
   p.causal = causal ? 1 : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = timeout_ns_from_env();
+  p.inject = inject_from_env();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int grid = static_cast<int>(units < ds->sms ? units : ds->sms);
+  // injected launch failure (tests only): an empty grid, which the launch rejects
+  const int grid = p.inject == 2 ? 0 : static_cast<int>(units < ds->sms ? units : ds->sms);
   cudaError_t e;
 #define ATTN_DEC_LAUNCH(DD, BB)                                                   \
   (Sq == 1 ? dec::launch_decode<DD, 1, BB>(p, grid, s)                          \

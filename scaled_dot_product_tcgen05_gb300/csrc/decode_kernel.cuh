@@ -58,6 +58,7 @@ struct DecParams {
   int causal;
   float scale_log2;          // scale * log2(e)
   long long timeout_ns;
+  int inject;                // fault injection for tests: 1 = block 0 skips its first fill
 };
 
 template <int D>
@@ -306,6 +307,9 @@ __device__ void dec_produce(const DecParams& p, uint32_t smem, uint32_t bars, co
       const uint32_t st = it % kStages;
       if (it >= kStages && !wait_bar(bars + 8u * (L::E + st), (it / kStages - 1) & 1u, ctl))
         return;
+      // injected fault (tests only): this fill never arrives, so the consumers'
+      // bounded wait runs out and the call reports ATTN_ERR_DEVICE_TIMEOUT
+      if (p.inject == 1 && blockIdx.x == 0 && it == 0) continue;
       const uint32_t full = bars + 8u * (L::F + st);
       ptx::mbar_arrive_expect_tx(full, 2 * L::kTile);
       const int row = w.b * p.Sk + w.k0 + j * kKeys;

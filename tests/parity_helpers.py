@@ -29,7 +29,8 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, row_mask=None, what=""):
     assert np.all(np.isfinite(o[sel_o])), f"{what}: non-finite O"
     lr, lg = lse_ref[sel_l], l[sel_l]
     both_inf = np.isneginf(lr) & np.isneginf(lg)
-    dl = np.where(both_inf, 0.0, np.abs(lg - lr) / np.maximum(1.0, np.abs(lr)))
+    with np.errstate(invalid="ignore"):  # -inf - -inf, masked by both_inf
+        dl = np.where(both_inf, 0.0, np.abs(lg - lr) / np.maximum(1.0, np.abs(lr)))
     stats = dict(o_max=float(d.max()), o_mean=float(d.mean()), lse_rel=float(np.nanmax(dl)),
                  n_o=int(d.size), n_lse=int(dl.size))
     assert stats["o_max"] <= O_MAX_ABS, f"{what}: O max-abs {stats}"
