@@ -268,8 +268,12 @@ int attn_num_sms(void);
 
 /*
  * attn_last_launch -- grid size (CTAs) and dynamic shared memory bytes of the
- * most recent attn_fwd launch on this thread; either pointer may be NULL.
- * Returns ATTN_OK, or ATTN_ERR_INVALID_ARG if nothing was launched yet.
+ * main kernel of the most recent launch by attn_fwd, attn_fwd_window,
+ * attn_fwd_decode, attn_bwd or attn_fwd_fp8 on this thread; either pointer may
+ * be NULL.  Returns ATTN_OK, or ATTN_ERR_INVALID_ARG if nothing was launched
+ * yet.  With ATTN_DEBUG=1 in the environment each such launch also prints one
+ * line ("attn: <entry point> grid=<CTAs> smem=<bytes>") to stderr; the library
+ * prints nothing otherwise.
  */
 int attn_last_launch(int* grid_ctas, int* smem_bytes);
 

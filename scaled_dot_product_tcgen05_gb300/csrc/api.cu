@@ -10,6 +10,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <mutex>
 
@@ -39,6 +40,16 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 thread_local int t_last_grid = -1;
 thread_local int t_last_smem = -1;
+
+// Records the shape of a launch for attn_last_launch; with ATTN_DEBUG=1 in the
+// environment also prints one line per launch to stderr (the library is
+// silent otherwise).
+void note_launch(const char* what, int grid, int smem) {
+  t_last_grid = grid;
+  t_last_smem = smem;
+  const char* dbg = std::getenv("ATTN_DEBUG");
+  if (dbg && dbg[0] == '1') std::fprintf(stderr, "attn: %s grid=%d smem=%d\n", what, grid, smem);
+}
 
 // Fault injection for the failure-detection tests, in attn_fwd_decode only:
 // ATTN_INJECT_FAULT=1 makes the decode kernel's block 0 skip its first fill,
@@ -214,8 +225,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     cudaGetLastError();
     return ATTN_ERR_CUDA;
   }
-  t_last_grid = info.grid;
-  t_last_smem = info.smem;
+  note_launch(window_left != -1 || window_right != -1 || global_q != 0 ? "attn_fwd_window"
+                                                                       : "attn_fwd",
+              info.grid, info.smem);
   return ATTN_OK;
 }
 
@@ -417,8 +429,8 @@ extern "C" int attn_fwd_decode(const void* q, const void* k_cache, const void* v
     cudaGetLastError();
     return ATTN_ERR_CUDA;
   }
-  t_last_grid = grid;
-  t_last_smem = D == 64 ? dec::DLayout<64>::kAlloc : dec::DLayout<128>::kAlloc;
+  note_launch("attn_fwd_decode", grid,
+              D == 64 ? dec::DLayout<64>::kAlloc : dec::DLayout<128>::kAlloc);
   return ATTN_OK;
 }
 
@@ -605,8 +617,7 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     cudaGetLastError();
     return ATTN_ERR_CUDA;
   }
-  t_last_grid = grid;
-  t_last_smem = D == 64 ? bwd::BLayout<64>::kAlloc : bwd::BLayout<128>::kAlloc;
+  note_launch("attn_bwd", grid, D == 64 ? bwd::BLayout<64>::kAlloc : bwd::BLayout<128>::kAlloc);
   return ATTN_OK;
 }
 
@@ -727,8 +738,7 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
     cudaGetLastError();
     return ATTN_ERR_CUDA;
   }
-  t_last_grid = grid;
-  t_last_smem = fp8::Layout8::kAlloc;
+  note_launch("attn_fwd_fp8", grid, fp8::Layout8::kAlloc);
   return ATTN_OK;
 }
 

@@ -107,3 +107,18 @@ def test_rejected_launch_returns_cuda_error_and_clears_it():
     assert st == pkg.ATTN_OK, pkg.status_string(st)
     o_ref, l_ref = attention_decode(q, k, v, None, 1 / math.sqrt(q.shape[-1]), True)
     compare(o, lse, o_ref, l_ref, what="decode after a rejected launch")
+
+
+@pytest.mark.gpu
+def test_debug_log_names_each_launch(capfd):
+    """ATTN_DEBUG=1: one stderr line per launch; silent otherwise."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    q, k, v = _decode_case()
+    _run_decode(q, k, v)
+    assert "attn:" not in capfd.readouterr().err
+    with _env(ATTN_DEBUG=1):
+        _run_decode(q, k, v)
+    err = capfd.readouterr().err
+    grid, smem = pkg.last_launch()
+    assert f"attn: attn_fwd_decode grid={grid} smem={smem}" in err, err
