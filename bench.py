@@ -10,9 +10,11 @@ exactly.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   (the fp64 CPU oracle on a bounded sample)
 
-Under torchrun each rank runs an independent replica on its own GPU (the
-forward has no cross-GPU exchange); the time is the max over ranks and the
-value counts the work of all ranks.  Rank 0 prints one JSON line.
+Under torchrun the job is N times the workload, sharded by whole batches: rank r
+processes shard r (the workload's shapes, its own seeded inputs) on its own GPU
+with no cross-GPU exchange (work units are independent); the time is the max
+over ranks and the value counts the work of all ranks (weak scaling).  Rank 0
+prints one JSON line.
 """
 from __future__ import annotations
 
@@ -52,6 +54,11 @@ def init_dist(backend: str):
     if ws > 1 and not torch.distributed.is_initialized():
         torch.distributed.init_process_group(backend=backend)
     return ws, rank
+
+
+def shard_workload(wl, rank: int):
+    """Shard ``rank`` of an N-times-larger job: the same shapes, its own inputs."""
+    return wl if rank == 0 else dataclasses.replace(wl, draw=wl.draw + 100 * rank)
 
 
 def max_over_ranks(x: float, device=None) -> float:
@@ -457,6 +464,7 @@ def main(argv=None):
     dev = torch.device("cuda", local)
     ws, rank = init_dist("nccl")
     pkg.load_library()
+    wl = shard_workload(wl, rank)
 
     inp = W.make_inputs(wl, pin=True)
     q_h, k_h, v_h = inp["q"], inp["k"], inp["v"]
@@ -645,7 +653,8 @@ def main(argv=None):
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_sample(wl, args.cpu_budget_s)
-    cfg = dict(cfg, parallelism=f"replicas x{ws}" if ws > 1 else "single GPU",
+    cfg = dict(cfg, parallelism=f"dp{ws}: rank r processes shard r (own inputs)" if ws > 1
+               else "single GPU",
                l2="no flush: inputs %.2f GiB > 129 MB L2" % (h2d / 2 ** 30),
                grid_ctas=grid, smem_bytes=smem)
     out = {

@@ -1,4 +1,4 @@
-"""Host-side logic of bench.py on the CPU: replica timing over ranks (gloo, 2 ranks),
+"""Host-side logic of bench.py on the CPU: sharded timing over ranks (gloo, 2 ranks),
 FLOP accounting and the reference-arm JSON contract."""
 import json
 import os
@@ -30,7 +30,9 @@ def _worker(rank, world, port, q):
     ws, r = bench.init_dist("gloo")
     t = bench.max_over_ranks(10.0 + 5.0 * rank)
     bench.barrier()
-    q.put((r, ws, t))
+    from scaled_dot_product_tcgen05_gb300 import workloads as W
+    wl = bench.shard_workload(W.standard_workloads()["long64k_causal"], r)
+    q.put((r, ws, t, wl.base_seed, (wl.B, wl.H, wl.Sq, wl.D)))
     dist.destroy_process_group()
 
 
@@ -45,7 +47,9 @@ def test_max_over_ranks_gloo_two_ranks():
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    assert got == [(0, 2, 15.0), (1, 2, 15.0)]
+    assert [g[:3] for g in got] == [(0, 2, 15.0), (1, 2, 15.0)]
+    # each rank processes its own shard: same shapes, distinct seeded inputs
+    assert got[0][4] == got[1][4] and got[0][3] != got[1][3]
 
 
 def test_max_over_ranks_single_process_is_identity():
@@ -125,3 +129,16 @@ def test_visible_key_counts_matches_a_direct_count():
                 n += ok
             want.append(n)
         assert np.array_equal(got, np.array(want))
+
+
+def test_shards_keep_shapes_and_draw_their_own_inputs():
+    from scaled_dot_product_tcgen05_gb300 import workloads as W
+    wl = W.standard_workloads()["bwd16k_causal"]
+    shards = [bench.shard_workload(wl, r) for r in range(8)]
+    assert shards[0] is wl
+    assert len({s.base_seed for s in shards}) == 8
+    assert all((s.B, s.H, s.Sq, s.Sk, s.D, s.causal, s.backward) ==
+               (wl.B, wl.H, wl.Sq, wl.Sk, wl.D, wl.causal, wl.backward) for s in shards)
+    # no shard's seed collides with another workload family's
+    others = {w.base_seed for n, w in W.standard_workloads().items() if w.wid != wl.wid}
+    assert not ({s.base_seed for s in shards} & others)
