@@ -273,9 +273,26 @@ __device__ __forceinline__ int unit_of(int k) {
 }
 
 // ---------------------------------------------------------------- softmax
-// Running state of one query row.  l_p sums the 16-bit P values that enter
-// P.V (it normalises O, so rounding of P cancels between numerator and
-// denominator); l_x sums the unrounded values (it gives the logsumexp).
+// x rounded to the 16-bit input type (nearest even) and back to fp32.
+template <bool BF16>
+__device__ __forceinline__ float round16(float x) {
+  const uint32_t pk = ptx::pack2<BF16>(x, 0.0f);  // x in the low half
+  float y;
+  if constexpr (BF16) {
+    y = __uint_as_float(pk << 16);
+  } else {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}"
+        : "=f"(y) : "r"(pk));
+  }
+  return y;
+}
+
+// Running state of one query row.  l_x sums the unrounded P values (it gives
+// the logsumexp).  l_p normalises O: the 16-bit kernels keep the same exact sum
+// plus, once per tile, the rounding error of the largest value a thread
+// writes (in a peaked row the largest values carry the rounding that shows
+// in O; the rounding of the rest averages out); the FP8 kernel sums the
+// rounded values themselves.
 struct RowState {
   float m;    // running max, log2 units (scale * log2e * s)
   float l_p;
@@ -325,7 +342,8 @@ __device__ __forceinline__ bool softmax_step_pv(uint32_t tS, uint32_t tO, int lo
     mx2 = ptx::max3(mx2, __uint_as_float(r[c + 4]), __uint_as_float(r[c + 5]));
     mx3 = ptx::max3(mx3, __uint_as_float(r[c + 6]), __uint_as_float(r[c + 7]));
   }
-  const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cle;
+  const float r_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));  // this row's largest score
+  const float m_tile = r_max * cle;
   const float m_new = fmaxf(st.m, m_tile);
   const bool rescale = m_new > st.m + kRescaleLog2;  // always true on the first tile
   const float m_use = rescale ? m_new : st.m;
@@ -333,10 +351,13 @@ __device__ __forceinline__ bool softmax_step_pv(uint32_t tS, uint32_t tO, int lo
   const float alpha = rescale ? ptx::ex2(st.m - m_safe) : 1.0f;
   st.m = m_use;
 
+  // the rounding error of the largest value, computed exactly as in the loop:
+  // it joins O's denominator
+  const float p_big = ptx::ex2(fmaf(r_max, cle, -m_safe));
+  const float corr = round16<BF16>(p_big) - p_big;
   const uint64_t cl2 = ptx::f2(cle, cle);
   const uint64_t nm2 = ptx::f2(-m_safe, -m_safe);
   uint64_t lx0 = ptx::f2(0.f, 0.f), lx1 = lx0;
-  float lp0 = 0.f, lp1 = 0.f, lp2 = 0.f, lp3 = 0.f;
   uint32_t pk[64];
 #pragma unroll
   for (int c = 0; c < 128; c += 4) {
@@ -350,17 +371,14 @@ __device__ __forceinline__ bool softmax_step_pv(uint32_t tS, uint32_t tO, int lo
     lx1 = ptx::f2_add(lx1, ptx::f2(p2, p3));
     pk[c / 2] = ptx::pack2<BF16>(p0, p1);
     pk[c / 2 + 1] = ptx::pack2<BF16>(p2, p3);
-    lp0 = ptx::add_lo16<BF16>(lp0, pk[c / 2]);
-    lp1 = ptx::add_hi16<BF16>(lp1, pk[c / 2]);
-    lp2 = ptx::add_lo16<BF16>(lp2, pk[c / 2 + 1]);
-    lp3 = ptx::add_hi16<BF16>(lp3, pk[c / 2 + 1]);
   }
   ptx::tmem_st_x64(tS, pk);
   float a0, a1, b0, b1;
   ptx::f2_split(lx0, a0, a1);
   ptx::f2_split(lx1, b0, b1);
-  st.l_x = st.l_x * alpha + ((a0 + a1) + (b0 + b1));
-  st.l_p = st.l_p * alpha + ((lp0 + lp1) + (lp2 + lp3));
+  const float sum = (a0 + a1) + (b0 + b1);
+  st.l_x = st.l_x * alpha + sum;
+  st.l_p = st.l_p * alpha + (sum + corr);
 
   if (!first && __any_sync(0xffffffffu, rescale)) {
     if (pvd_bar != 0) {

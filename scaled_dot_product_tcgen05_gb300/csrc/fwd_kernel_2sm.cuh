@@ -117,20 +117,6 @@ __device__ __forceinline__ bool decode_pair(const FwdParams& p, int k, Cursor& c
 }
 
 // ---------------------------------------------------------------- softmax
-// x rounded to the 16-bit input type (nearest even) and back to fp32.
-template <bool BF16>
-__device__ __forceinline__ float round16(float x) {
-  const uint32_t pk = ptx::pack2<BF16>(x, 0.0f);  // x in the low half
-  float y;
-  if constexpr (BF16) {
-    y = __uint_as_float(pk << 16);
-  } else {
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}"
-        : "=f"(y) : "r"(pk));
-  }
-  return y;
-}
-
 // One K/V step of the online softmax for half of a query row: this thread owns
 // keys [64h, 64h+64) of S (the other half sits with the thread of the same lane
 // in warp w ^ 4, on the same SM sub-partition and TMEM lane quarter).  The two
