@@ -282,6 +282,35 @@ def attention_backward_dense(q, k, v, do, scale: float, causal: bool,
     return dq, dk, dv
 
 
+def attention_backward_sampled(q, k, v, do, scale: float, causal: bool, q_rows, k_rows):
+    """dQ at the query rows ``q_rows`` and dK, dV at the key rows ``k_rows`` of one
+    (sequence, head), for sequences too long to form every score.
+
+    The same definitions as attention_backward_one_head (page "Multi-Head
+    Attention的计算本质与性能瓶颈", §3.3, the chain rule through the forward),
+    evaluated on the score rows these outputs need: the rows ``q_rows`` and
+    every query row that sees one of the keys ``k_rows`` (under causal masking,
+    for keys near the end of the sequence, a few rows).  Returns dQ
+    [len(q_rows), D], dK [len(k_rows), D], dV [len(k_rows), Dv] in fp64.
+    """
+    q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+    Sq, Sk = q.shape[0], k.shape[0]
+    q_rows = np.asarray(q_rows, dtype=np.int64)
+    k_rows = np.asarray(k_rows, dtype=np.int64)
+    sees = np.zeros(Sq, dtype=bool)
+    for r0 in range(0, Sq, 1024):  # the query rows that see one of the keys
+        rr = np.arange(r0, min(Sq, r0 + 1024))
+        sees[rr] = visible_mask(rr, Sk, causal)[:, k_rows].any(axis=1)
+    rows = np.union1d(q_rows, np.nonzero(sees)[0])
+    _, _, p = attention_one_head(q, k, v, scale, causal, rows=rows, return_p=True)
+    dp = do[rows] @ v.T
+    ds = p * (dp - (dp * p).sum(axis=1, keepdims=True))
+    at = np.searchsorted(rows, q_rows)
+    dq = scale * (ds[at] @ k)
+    dk = scale * (ds[:, k_rows].T @ q[rows])
+    dv = p[:, k_rows].T @ do[rows]
+    return dq, dk, dv
+
 def attention_backward_varlen(q, k, v, do, cu_seqlens_q, cu_seqlens_k, scale: float,
                               causal: bool, heads: Optional[Sequence[int]] = None):
     """Packed varlen batch: q/do [Tq,H,D], k/v [Tk,H,D] -> dQ, dK, dV in the same layouts.

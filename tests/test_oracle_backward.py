@@ -12,7 +12,8 @@ import pytest
 import torch
 
 from oracle.sdpa_oracle import (attention_backward_dense, attention_backward_one_head,
-                                attention_backward_varlen, attention_one_head)
+                                attention_backward_sampled, attention_backward_varlen,
+                                attention_one_head)
 
 
 def _rng(seed):
@@ -223,3 +224,38 @@ def test_varlen_matches_torch_autograd_on_a_ragged_batch():
     o.backward(torch.from_numpy(do.transpose(1, 0, 2)))
     for x, t in zip(g, (qt, kt, vt)):
         np.testing.assert_allclose(x, t.grad.numpy().transpose(1, 0, 2), rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------- sampled outputs
+@pytest.mark.parametrize("causal,Sq,Sk", [(True, 37, 37), (False, 29, 41), (True, 30, 45),
+                                          (False, 40, 23)])
+def test_sampled_backward_equals_the_full_backward(causal, Sq, Sk):
+    """dQ at sampled rows and dK, dV at sampled keys from the needed score rows only equal
+    the full backward at those rows and keys."""
+    r = _rng(41 + Sq)
+    D = 5
+    q, do = r.normal(size=(Sq, D)), r.normal(size=(Sq, D + 1))
+    k, v = r.normal(size=(Sk, D)), r.normal(size=(Sk, D + 1))
+    full = attention_backward_one_head(q, k, v, do, 0.45, causal)
+    q_rows = np.array([0, 3, Sq // 2, Sq - 1])
+    k_rows = np.array([Sk - 1, Sk - 5, Sk // 3])
+    dq, dk, dv = attention_backward_sampled(q, k, v, do, 0.45, causal, q_rows, k_rows)
+    np.testing.assert_allclose(dq, full[0][q_rows], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, full[1][k_rows], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, full[2][k_rows], rtol=0, atol=1e-12)
+
+
+def test_sampled_backward_reads_only_the_rows_it_needs():
+    """Causal, keys at the end: changing queries (and their dO) that see none of the sampled
+    keys and are not sampled themselves leaves the sampled outputs unchanged."""
+    r = _rng(47)
+    S, D = 60, 4
+    q, k, v, do = (r.normal(size=(S, D)) for _ in range(4))
+    q_rows, k_rows = np.array([2, 5]), np.array([55, 58])
+    a = attention_backward_sampled(q, k, v, do, 0.6, True, q_rows, k_rows)
+    q2, do2 = q.copy(), do.copy()
+    q2[10:50] += 3.0   # rows 10..49 see no key >= 55 and are not sampled
+    do2[10:50] -= 1.0
+    b = attention_backward_sampled(q2, k, v, do2, 0.6, True, q_rows, k_rows)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
