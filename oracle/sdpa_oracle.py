@@ -293,7 +293,7 @@ def attention_backward_sampled(q, k, v, do, scale: float, causal: bool, q_rows, 
     for keys near the end of the sequence, a few rows).  Returns dQ
     [len(q_rows), D], dK [len(k_rows), D], dV [len(k_rows), Dv] in fp64.
     """
-    q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+    q, k, v, do = (_as_f64(x) for x in (q, k, v, do))
     Sq, Sk = q.shape[0], k.shape[0]
     q_rows = np.asarray(q_rows, dtype=np.int64)
     k_rows = np.asarray(k_rows, dtype=np.int64)

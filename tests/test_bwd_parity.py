@@ -258,3 +258,24 @@ def test_bwd_many_units_per_cta_packed():
     heads = [1, 6]
     ref = attention_backward_varlen(q, k, v, do, cq, ck, scale, True, heads=heads)
     compare_grads([g[:, heads] for g in got], [r[:, heads] for r in ref], "packed 600 units")
+
+
+def test_bwd_full_size_sampled():
+    """The benchmarked problem (B=1 H=32 S=16384 D=128 bf16 causal) in the bench's launch
+    configuration: dQ at seeded query rows and dK, dV at the last keys of two heads, from
+    the oracle's sampled backward."""
+    from oracle.sdpa_oracle import attention_backward_sampled
+    from scaled_dot_product_tcgen05_gb300 import workloads as W
+    wl = W.standard_workloads()["bwd16k_causal"]
+    inp = W.make_inputs(wl)
+    q, k, v, do = inp["q"], inp["k"], inp["v"], inp["do"]
+    got = _run(q, k, v, do, True, wl.scale)
+    S = wl.Sq
+    rng = np.random.default_rng(16384)
+    q_rows = np.union1d(rng.choice(S, 24, replace=False), [0, 1, 127, 128, 8191, S - 1])
+    k_rows = np.union1d(np.arange(S - 64, S), [S - 129, S - 1000])
+    for h in (0, 17):
+        ref = attention_backward_sampled(q[0, :, h], k[0, :, h], v[0, :, h], do[0, :, h],
+                                         wl.scale, True, q_rows, k_rows)
+        sub = [got[0][0, q_rows, h], got[1][0, k_rows, h], got[2][0, k_rows, h]]
+        compare_grads(sub, list(ref), f"bwd16k head {h}")
