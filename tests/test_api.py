@@ -176,3 +176,14 @@ def test_bwd_rejects_zero_scale_and_bad_sizes(lib):
     assert lib.attn_bwd_workspace(5, 2, 300, 128, 1, ctypes.byref(n)) == pkg.ATTN_OK
     assert n.value == ((2 * 300 * 128 * 4 + 255) // 256) * 256 + 2 * 7 * 8192 + 256
     assert lib.attn_bwd_workspace(1, 2, 300, 96, 0, ctypes.byref(n)) == pkg.ATTN_ERR_UNSUPPORTED
+
+def test_fp8_workspace_is_the_transposed_v_with_keys_padded_to_16(lib):
+    n = ctypes.c_size_t(0)
+    for B, H, Sk, keys in ((1, 2, 16, 16), (2, 3, 17, 32), (1, 32, 65536, 65536), (3, 1, 1, 16)):
+        assert lib.attn_fwd_fp8_workspace(B, H, Sk, 128, ctypes.byref(n)) == pkg.ATTN_OK
+        assert n.value == H * 128 * B * keys  # V^T [H, 128, B * round16(Sk)], one byte each
+    assert lib.attn_fwd_fp8_workspace(1, 2, 16, 64, ctypes.byref(n)) == pkg.ATTN_ERR_UNSUPPORTED
+    assert n.value == 0
+    assert lib.attn_fwd_fp8_workspace(1, 0, 16, 128, ctypes.byref(n)) == pkg.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_fp8_workspace(1, 2, 0, 128, ctypes.byref(n)) == pkg.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_fp8_workspace(1, 2, 16, 128, None) == pkg.ATTN_ERR_INVALID_ARG
