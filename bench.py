@@ -7,7 +7,7 @@ FLOP count 4*B*H*Sq*Sk*D, halved for causal; for a sliding-window workload
 (--workload window128k_causal) 4*D per visible (query, key) pair, counted
 exactly.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--seed S]
   python bench.py --impl reference ...   (the fp64 CPU oracle on a bounded sample)
 
 Under torchrun the job is N times the workload, sharded by whole batches: rank r
@@ -54,6 +54,13 @@ def init_dist(backend: str):
     if ws > 1 and not torch.distributed.is_initialized():
         torch.distributed.init_process_group(backend=backend)
     return ws, rank
+
+
+def reseed_workload(wl, seed: int):
+    """The same workload with another seeded draw (seed 0: unchanged)."""
+    if not 0 <= seed < 10:
+        raise SystemExit("--seed must be in 0..9 (the draws of a workload family)")
+    return wl if seed == 0 else dataclasses.replace(wl, draw=wl.draw + 10 * seed)
 
 
 def shard_workload(wl, rank: int):
@@ -441,12 +448,16 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=192)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed", type=int, default=0,
+                    help="another seeded draw of the same workload (0: the standard draw)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    wl = W.standard_workloads()[args.workload]
+    wl = reseed_workload(W.standard_workloads()[args.workload], args.seed)
     flops, nbytes, cfg = workload_info(wl)
+    if args.seed:
+        cfg = dict(cfg, seed=args.seed)
     ws, rank, local = dist_env()
 
     if args.impl == "reference":

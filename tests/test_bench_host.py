@@ -142,3 +142,21 @@ def test_shards_keep_shapes_and_draw_their_own_inputs():
     # no shard's seed collides with another workload family's
     others = {w.base_seed for n, w in W.standard_workloads().items() if w.wid != wl.wid}
     assert not ({s.base_seed for s in shards} & others)
+
+
+def test_seed_selects_another_draw_of_the_same_workload():
+    from scaled_dot_product_tcgen05_gb300 import workloads as W
+    wl = W.standard_workloads()["long64k_causal"]
+    assert bench.reseed_workload(wl, 0) is wl
+    seeds = [bench.reseed_workload(wl, s) for s in range(10)]
+    assert len({s.base_seed for s in seeds}) == 10
+    assert all((s.B, s.H, s.Sq, s.D, s.causal) == (wl.B, wl.H, wl.Sq, wl.D, wl.causal)
+               for s in seeds)
+    # reseeded and sharded draws of every workload stay inside its family's seed block
+    for w in W.standard_workloads().values():
+        for s in range(10):
+            for r in range(8):
+                x = bench.shard_workload(bench.reseed_workload(w, s), r)
+                assert x.base_seed // 1000 == w.wid
+    with pytest.raises(SystemExit):
+        bench.reseed_workload(wl, 10)
