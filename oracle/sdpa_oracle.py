@@ -234,7 +234,8 @@ def merge_partials(o_parts, lse_parts):
     return out, lse
 
 
-def attention_backward_one_head(q, k, v, do, scale: float, causal: bool):
+def attention_backward_one_head(q, k, v, do, scale: float, causal: bool, o=None,
+                                return_terms: bool = False):
     """Gradients of attention for one (sequence, head): returns dQ, dK, dV.
 
     q [Sq, D], k [Sk, D], v [Sk, Dv], do = dL/dO [Sq, Dv], fp64.  The forward is
@@ -250,26 +251,41 @@ def attention_backward_one_head(q, k, v, do, scale: float, causal: bool):
         dQ = scale * dS K,   dK = scale * dS^T Q
     Masked entries have P = 0 and so no gradient; a row with no visible key
     contributes nothing.
+
+    A backward is handed the forward's output O as an input; since
+    rowsum(dP * P) = rowsum(dO * O) for the exact O, the row term may be taken
+    from it.  ``o`` (optional, [Sq, Dv]) is such a caller-provided O: the row
+    term becomes rowsum(dO * o), i.e. the gradient a backward computes from
+    the O it was given (with ``o`` equal to the exact O, the gradient above).
+    ``return_terms`` also returns P and dS (the terms that error bounds of an
+    implementation are built from).
     """
     q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
     Sq, Sk = q.shape[0], k.shape[0]
     _, _, p = attention_one_head(q, k, v, scale, causal, return_p=True)
     dv = p.T @ do
     dp = do @ v.T
-    row = (dp * p).sum(axis=1, keepdims=True)
+    if o is None:
+        row = (dp * p).sum(axis=1, keepdims=True)
+    else:
+        row = (do * np.asarray(o, dtype=np.float64)).sum(axis=1, keepdims=True)
     ds = p * (dp - row)
     dq = scale * (ds @ k)
     dk = scale * (ds.T @ q)
+    if return_terms:
+        return dq, dk, dv, p, ds
     return dq, dk, dv
 
 
 def attention_backward_dense(q, k, v, do, scale: float, causal: bool,
-                             heads: Optional[Sequence[int]] = None):
+                             heads: Optional[Sequence[int]] = None, o=None):
     """Dense batch: q/do [B,Sq,H,D], k/v [B,Sk,H,D] -> dQ, dK, dV in the same layouts.
 
-    Heads not listed in ``heads`` are NaN.
+    Heads not listed in ``heads`` are NaN.  ``o`` [B,Sq,H,Dv]: the caller's
+    forward output for the row term (see attention_backward_one_head).
     """
     q, k, v, do = (_as_f64(x) for x in (q, k, v, do))
+    o = None if o is None else _as_f64(o)
     B, Sq, H, D = q.shape
     dq = np.full(q.shape, np.nan)
     dk = np.full(k.shape, np.nan)
@@ -277,12 +293,14 @@ def attention_backward_dense(q, k, v, do, scale: float, causal: bool,
     for b in range(B):
         for h in (range(H) if heads is None else heads):
             g = attention_backward_one_head(q[b, :, h], k[b, :, h], v[b, :, h], do[b, :, h],
-                                            scale, causal)
+                                            scale, causal,
+                                            o=None if o is None else o[b, :, h])
             dq[b, :, h], dk[b, :, h], dv[b, :, h] = g
     return dq, dk, dv
 
 
-def attention_backward_sampled(q, k, v, do, scale: float, causal: bool, q_rows, k_rows):
+def attention_backward_sampled(q, k, v, do, scale: float, causal: bool, q_rows, k_rows,
+                               return_terms: bool = False):
     """dQ at the query rows ``q_rows`` and dK, dV at the key rows ``k_rows`` of one
     (sequence, head), for sequences too long to form every score.
 
@@ -291,7 +309,8 @@ def attention_backward_sampled(q, k, v, do, scale: float, causal: bool, q_rows, 
     evaluated on the score rows these outputs need: the rows ``q_rows`` and
     every query row that sees one of the keys ``k_rows`` (under causal masking,
     for keys near the end of the sequence, a few rows).  Returns dQ
-    [len(q_rows), D], dK [len(k_rows), D], dV [len(k_rows), Dv] in fp64.
+    [len(q_rows), D], dK [len(k_rows), D], dV [len(k_rows), Dv] in fp64; with
+    ``return_terms`` also the score rows used, their P and dS, and their O.
     """
     q, k, v, do = (_as_f64(x) for x in (q, k, v, do))
     Sq, Sk = q.shape[0], k.shape[0]
@@ -309,10 +328,12 @@ def attention_backward_sampled(q, k, v, do, scale: float, causal: bool, q_rows, 
     dq = scale * (ds[at] @ k)
     dk = scale * (ds[:, k_rows].T @ q[rows])
     dv = p[:, k_rows].T @ do[rows]
+    if return_terms:
+        return dq, dk, dv, rows, p, ds, p @ v
     return dq, dk, dv
 
 def attention_backward_varlen(q, k, v, do, cu_seqlens_q, cu_seqlens_k, scale: float,
-                              causal: bool, heads: Optional[Sequence[int]] = None):
+                              causal: bool, heads: Optional[Sequence[int]] = None, o=None):
     """Packed varlen batch: q/do [Tq,H,D], k/v [Tk,H,D] -> dQ, dK, dV in the same layouts.
 
     Sequence b's queries cu_seqlens_q[b]:cu_seqlens_q[b+1] see only its keys
@@ -320,9 +341,11 @@ def attention_backward_varlen(q, k, v, do, cu_seqlens_q, cu_seqlens_k, scale: fl
     gradients are those of attention_backward_one_head on its slices.  A
     sequence without queries gives its keys zero dK and dV; one without keys
     gives its queries zero dQ.  Rows that belong to no sequence, and heads not
-    listed in ``heads``, are NaN.
+    listed in ``heads``, are NaN.  ``o`` [Tq,H,Dv]: the caller's forward output
+    for the row term (see attention_backward_one_head).
     """
     q, k, v, do = (_as_f64(x) for x in (q, k, v, do))
+    o = None if o is None else _as_f64(o)
     cq = [int(x) for x in np.asarray(cu_seqlens_q).tolist()]
     ck = [int(x) for x in np.asarray(cu_seqlens_k).tolist()]
     dq = np.full(q.shape, np.nan)
@@ -338,6 +361,7 @@ def attention_backward_varlen(q, k, v, do, cu_seqlens_q, cu_seqlens_k, scale: fl
                 dv[k0:k1, h] = 0.0
                 continue
             g = attention_backward_one_head(q[q0:q1, h], k[k0:k1, h], v[k0:k1, h],
-                                            do[q0:q1, h], scale, causal)
+                                            do[q0:q1, h], scale, causal,
+                                            o=None if o is None else o[q0:q1, h])
             dq[q0:q1, h], dk[k0:k1, h], dv[k0:k1, h] = g
     return dq, dk, dv

@@ -259,3 +259,84 @@ def test_sampled_backward_reads_only_the_rows_it_needs():
     b = attention_backward_sampled(q2, k, v, do2, 0.6, True, q_rows, k_rows)
     for x, y in zip(a, b):
         np.testing.assert_array_equal(x, y)
+
+
+# ------------------------------------------------- the caller's forward output
+def test_row_term_from_the_exact_output_is_the_gradient():
+    """rowsum(dP * P) = rowsum(dO * O) for the exact O, so handing the oracle's own
+    forward output as the caller's O reproduces the autograd-pinned gradient."""
+    for seed, (Sq, Sk, D, causal) in enumerate([(9, 9, 5, True), (6, 11, 3, False),
+                                                (12, 12, 8, True)]):
+        r = _rng(40 + seed)
+        q, k, v = r.normal(size=(Sq, D)), r.normal(size=(Sk, D)), r.normal(size=(Sk, D + 1))
+        do = r.normal(size=(Sq, D + 1))
+        o, _ = attention_one_head(q, k, v, 0.6, causal)
+        ref = _torch_grads(q, k, v, do, 0.6, causal)
+        got = attention_backward_one_head(q, k, v, do, 0.6, causal, o=o)
+        for g, rr in zip(got, ref):
+            np.testing.assert_allclose(g, rr, rtol=0, atol=1e-11)
+
+
+def test_gradient_is_affine_in_the_callers_output_and_dv_ignores_it():
+    """The caller's O enters only through the row term, linearly: equal steps in O give
+    equal steps in dQ and dK, and dV does not depend on it."""
+    r = _rng(50)
+    Sq, Sk, D = 10, 13, 6
+    q, k, v, do = r.normal(size=(Sq, D)), r.normal(size=(Sk, D)), r.normal(size=(Sk, D)), \
+        r.normal(size=(Sq, D))
+    o, _ = attention_one_head(q, k, v, 0.4, True)
+    step = r.normal(size=o.shape) * 1e-2
+    g0, g1, g2 = (attention_backward_one_head(q, k, v, do, 0.4, True, o=o + t * step)
+                  for t in (0.0, 1.0, 2.0))
+    for i in (0, 1):
+        np.testing.assert_allclose(g2[i] - g1[i], g1[i] - g0[i], rtol=0, atol=1e-13)
+        assert np.abs(g1[i] - g0[i]).max() > 1e-6  # the row term does move them
+    np.testing.assert_array_equal(g0[2], g1[2])
+
+
+def test_returned_terms_reproduce_the_gradients():
+    """P and dS returned by the oracle are the terms of its own products."""
+    r = _rng(60)
+    Sq, Sk, D = 8, 8, 4
+    q, k, v, do = (r.normal(size=(S, D)) for S in (Sq, Sk, Sk, Sq))
+    dq, dk, dv, p, ds = attention_backward_one_head(q, k, v, do, 0.7, True, return_terms=True)
+    np.testing.assert_allclose(p.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    assert np.all(np.triu(p, 1) == 0) and np.all(np.triu(ds, 1) == 0)  # causal: masked
+    np.testing.assert_allclose(dq, 0.7 * ds @ k, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, 0.7 * ds.T @ q, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, p.T @ do, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ds.sum(axis=1), 0.0, rtol=0, atol=1e-12)  # softmax Jacobian rows
+
+
+def test_dense_and_packed_wrappers_pass_the_callers_output():
+    r = _rng(70)
+    B, S, H, D = 2, 9, 2, 4
+    q, k, v, do = (r.normal(size=(B, S, H, D)) for _ in range(4))
+    o = r.normal(size=(B, S, H, D))
+    dense = attention_backward_dense(q, k, v, do, 0.5, True, o=o)
+    one = attention_backward_one_head(q[1, :, 1], k[1, :, 1], v[1, :, 1], do[1, :, 1], 0.5, True,
+                                      o=o[1, :, 1])
+    for a, b in zip(dense, one):
+        np.testing.assert_array_equal(a[1, :, 1], b)
+    cu = np.array([0, S, 2 * S], dtype=np.int32)
+    flat = lambda x: x.reshape(B * S, H, D)  # noqa: E731
+    packed = attention_backward_varlen(flat(q), flat(k), flat(v), flat(do), cu, cu, 0.5, True,
+                                       o=flat(o))
+    for a, b in zip(dense, packed):
+        np.testing.assert_allclose(flat(a), b, rtol=0, atol=1e-13)
+
+
+def test_sampled_backward_terms_are_the_full_terms_at_its_rows():
+    r = _rng(80)
+    Sq = Sk = 40
+    D = 5
+    q, k, v, do = (r.normal(size=(Sq, D)) for _ in range(4))
+    dq, dk, dv, p, ds = attention_backward_one_head(q, k, v, do, 0.5, True, return_terms=True)
+    o_full, _ = attention_one_head(q, k, v, 0.5, True)
+    q_rows, k_rows = np.array([1, 17, 39]), np.array([30, 39])
+    _, _, _, rows, p_s, ds_s, o_s = attention_backward_sampled(q, k, v, do, 0.5, True, q_rows,
+                                                               k_rows, return_terms=True)
+    assert set(q_rows) <= set(rows) and set(range(30, 40)) <= set(rows)
+    np.testing.assert_allclose(p_s, p[rows], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(ds_s, ds[rows], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(o_s, o_full[rows], rtol=0, atol=1e-13)
