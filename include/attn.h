@@ -69,7 +69,10 @@ typedef enum { ATTN_DTYPE_FP16 = 0, ATTN_DTYPE_BF16 = 1 } attn_dtype;
  *   stream    cudaStream_t (passed as void*), NULL = legacy default stream.
  *
  * Errors: argument, alignment, dtype and device errors are returned before
- * anything is launched and leave o/lse untouched.  Launch failures return
+ * anything is launched and leave o/lse untouched.  Each pointer is checked to
+ * be device (or managed) memory of the current device; a pointer that passed
+ * the check is remembered per thread (the last 16), so the check tests where a
+ * buffer lives, not whether it is still allocated.  Launch failures return
  * ATTN_ERR_CUDA.  Problems found on the device (a bad cu_seqlens array, a
  * pipeline wait past its limit) set a per-device error word that attn_check
  * reports; outputs of that call are then undefined.
@@ -246,14 +249,19 @@ int attn_fwd_fp8_workspace(int B, int H, int Sk, int D, size_t* bytes);
  * attn_check -- synchronise `stream`, then report and clear the device error
  * word of the current device: ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT,
  * ATTN_ERR_BAD_SEQLENS, or ATTN_ERR_CUDA if the stream itself failed.
+ * The error word is one per device, not per stream: every call of the
+ * allocating entry points on that device reports into it, so an error raised
+ * by a kernel on another stream (that has finished by then) is reported too,
+ * to whichever caller checks first, and is cleared by that check.
  *
  * Debug environment (read at every call): ATTN_WAIT_TIMEOUT_MS bounds every
  * device-side wait (default 5000); when one runs out the kernel sets the
  * error word, its roles drain and it exits, leaving the context usable.
- * ATTN_INJECT_FAULT (tests only, attn_fwd_decode): 1 = the first tile fill of
- * block 0 is skipped, so that a wait runs out (ATTN_ERR_DEVICE_TIMEOUT from
- * attn_check); 2 = the kernel is launched with an empty grid, which the
- * launch rejects (the call returns ATTN_ERR_CUDA).
+ * ATTN_INJECT_FAULT (tests only): 1 = block 0 of the forward kernels
+ * (attn_fwd, attn_fwd_window) skips its first K tile, block 0 of the decode
+ * kernel its first tile fill, so that a wait runs out (ATTN_ERR_DEVICE_TIMEOUT
+ * from attn_check); 2 = attn_fwd_decode launches its kernel with an empty
+ * grid, which the launch rejects (the call returns ATTN_ERR_CUDA).
  */
 int attn_check(void* stream);
 
@@ -292,6 +300,8 @@ int attn_last_launch(int* grid_ctas, int* smem_bytes);
  *                  and device-side errors are not reported.  Non-NULL: the call
  *                  waits for `stream` and stores ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT
  *                  or ATTN_ERR_BAD_SEQLENS there.
+ * Device-side waits are bounded as in attn_fwd (ATTN_WAIT_TIMEOUT_MS, read at
+ * every call; see attn_check).
  * The scratch needed by a call (one error word, any problem size) is checked
  * against the array's 256 bytes; a call needing more returns
  * ATTN_ERR_INVALID_ARG.  All calls on a device share the array and it keeps the
@@ -306,9 +316,11 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float
                      int dtype, void* stream, int* device_status);
 
 /*
- * attn_release -- free the library-owned per-device state (the error word) of
- * every device it was created on.  Call only when no attn_fwd launch is in
- * flight.  Later calls recreate the state.
+ * attn_release -- free the library-owned per-device state of every device it
+ * was created on: the device error word that attn_fwd, attn_fwd_window,
+ * attn_fwd_decode, attn_merge, attn_bwd and attn_fwd_fp8 report into (see
+ * attn_check), and the record of device pointers already checked.  Call only
+ * when none of their launches is in flight.  Later calls recreate the state.
  */
 int attn_release(void);
 

@@ -16,6 +16,7 @@
 
 #include "attn.h"
 #include "bwd_kernel.cuh"
+#include "host_common.h"
 #include "decode_kernel.cuh"
 #include "fwd_fp8_kernel.cuh"
 #include "launch.cuh"
@@ -25,18 +26,24 @@ namespace attn {
 
 namespace {
 
-constexpr int kMaxDevices = 64;
+using host::aligned;
+using host::encode_rows_heads_dim;
+using host::inject_from_env;
+using host::kMaxDevices;
+using host::on_device;
+using host::timeout_ns_from_env;
 
+// Per-device state of the allocating entry points: the SM count and the
+// device error word the kernels report into (one per device, shared by every
+// stream and every call on that device; allocated on first use, freed by
+// attn_release).
 struct DeviceState {
-  bool ready = false;
-  bool supported = false;
   int sms = 0;
-  int* err = nullptr;  // device error word
+  int* err = nullptr;
 };
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 thread_local int t_last_grid = -1;
 thread_local int t_last_smem = -1;
@@ -51,83 +58,28 @@ void note_launch(const char* what, int grid, int smem) {
   if (dbg && dbg[0] == '1') std::fprintf(stderr, "attn: %s grid=%d smem=%d\n", what, grid, smem);
 }
 
-// Fault injection for the failure-detection tests, in attn_fwd_decode only:
-// ATTN_INJECT_FAULT=1 makes the decode kernel's block 0 skip its first fill,
-// so a bounded wait runs out; =2 launches an empty grid, which the launch
-// rejects.  Unset in normal use.
-int inject_from_env() {
-  const char* s = std::getenv("ATTN_INJECT_FAULT");
-  return s ? std::atoi(s) : 0;
-}
-
-long long timeout_ns_from_env() {
-  const char* s = std::getenv("ATTN_WAIT_TIMEOUT_MS");
-  long long ms = s ? std::atoll(s) : 0;
-  if (ms <= 0) ms = 5000;
-  return ms * 1000000LL;
-}
-
-// Creates the per-device state on first use.  Returns ATTN_OK or an error.
+// The per-device state on first use (an sm_103 device; the error word is
+// allocated here).  Returns ATTN_OK or an error.
 int device_state(int dev, DeviceState** out) {
-  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  const host::DeviceInfo* info = nullptr;
+  const int st = host::device_info(dev, &info);
+  if (st != ATTN_OK) return st;
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState& s = g_dev[dev];
-  if (!s.ready) {
-    int major = 0, minor = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+  if (!s.err) {
+    if (cudaMalloc(&s.err, sizeof(int)) != cudaSuccess) {
+      s.err = nullptr;
+      cudaGetLastError();
       return ATTN_ERR_CUDA;
-    s.supported = (major == 10 && minor == 3);
-    s.sms = sms;
-    if (s.supported) {
-      if (!g_encode) {
-        cudaDriverEntryPointQueryResult q;
-        void* fn = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || fn == nullptr)
-          return ATTN_ERR_CUDA;
-        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-      }
-      if (cudaMalloc(&s.err, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
-      if (cudaMemset(s.err, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
     }
-    s.ready = true;
+    if (cudaMemset(s.err, 0, sizeof(int)) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
   }
-  if (!s.supported) return ATTN_ERR_UNSUPPORTED;
+  s.sms = info->sms;
   *out = &s;
   return ATTN_OK;
-}
-
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// The pointer must be device (or managed) memory reachable from `dev`.
-bool on_device(const void* p, int dev) {
-  cudaPointerAttributes a;
-  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  if (a.type == cudaMemoryTypeManaged) return true;
-  return a.type == cudaMemoryTypeDevice && a.device == dev;
-}
-
-// [rows, H, D] 16-bit tensor, box = box_rows rows x 1 head x 64 elements
-// (128 B), 128-byte swizzle, zero fill outside the tensor.
-int encode_rows_heads_dim(CUtensorMap* m, const void* ptr, long long rows, int H, int D,
-                          bool bf16, int box_rows = kBM) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
-                        static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
-                           static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(D) * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                        3, const_cast<void*>(ptr), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 // The backward's fp32 dQ accumulator [slices, rows, D] as a 3-D map {D, rows,
@@ -141,7 +93,7 @@ int encode_dq_acc(CUtensorMap* m, float* ptr, int slices, int rows, int D) {
                            static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(D) * 4};
   cuuint32_t box[3] = {32, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+  CUresult r = host::encoder_slot()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
@@ -159,68 +111,24 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
              int Sq, int Sk, int D, float scale, int causal, int window_left, int window_right,
              int global_q, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int dtype,
              void* stream) {
-  // ---- argument checks (no CUDA call before these pass)
-  if (B < 0 || H < 1 || Sq < 0 || Sk < 1) return ATTN_ERR_INVALID_ARG;
   FwdParams p;
-  if (!set_mask(p, causal, window_left, window_right, global_q)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  if (dtype != ATTN_DTYPE_FP16 && dtype != ATTN_DTYPE_BF16) return ATTN_ERR_UNSUPPORTED;
-  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  const bool varlen = cu_seqlens_q != nullptr || cu_seqlens_k != nullptr;
-  if (varlen && (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr)) return ATTN_ERR_INVALID_ARG;
-  if (B == 0 || Sq == 0) return ATTN_OK;
-  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
-    return ATTN_ERR_MISALIGNED;
-  if (varlen && (!aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4))) return ATTN_ERR_MISALIGNED;
-  const long long rows_q = varlen ? Sq : static_cast<long long>(B) * Sq;
-  const long long rows_k = varlen ? Sk : static_cast<long long>(B) * Sk;
-  if (rows_q > INT_MAX - 2 * kUnitRows || rows_k > INT_MAX - 2 * kBN) return ATTN_ERR_INVALID_ARG;
-  // unit indices are int: B*H*ceil(Sq/256) (dense) or H*(ceil(Sq/256)+B) (varlen)
-  const long long units_bound = varlen
-      ? static_cast<long long>(H) * ((rows_q + kUnitRows - 1) / kUnitRows + B)
-      : static_cast<long long>(B) * H * ((Sq + kUnitRows - 1) / kUnitRows);
-  if (units_bound > INT_MAX / 2) return ATTN_ERR_INVALID_ARG;
-
-  // ---- device checks
+  host::FwdCall call;
+  int st = host::check_fwd_args(q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, window_left,
+                                window_right, global_q, cu_seqlens_q, cu_seqlens_k, dtype, &p,
+                                &call);
+  if (st != ATTN_OK || call.nothing) return st;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    return ATTN_ERR_CUDA;
-  }
+  if ((st = host::current_device(&dev)) != ATTN_OK) return st;
   DeviceState* ds = nullptr;
-  int st = device_state(dev, &ds);
-  if (st != ATTN_OK) return st;
-  if (!on_device(q, dev) || !on_device(k, dev) || !on_device(v, dev) || !on_device(o, dev) ||
-      !on_device(lse, dev))
-    return ATTN_ERR_INVALID_ARG;
-  if (varlen && (!on_device(cu_seqlens_q, dev) || !on_device(cu_seqlens_k, dev)))
-    return ATTN_ERR_INVALID_ARG;
-
-  // ---- parameters
-  const bool bf16 = dtype == ATTN_DTYPE_BF16;
-  if (encode_rows_heads_dim(&p.tm_q, q, rows_q, H, D, bf16) != ATTN_OK ||
-      encode_rows_heads_dim(&p.tm_k, k, rows_k, H, D, bf16) != ATTN_OK ||
-      encode_rows_heads_dim(&p.tm_v, v, rows_k, H, D, bf16) != ATTN_OK ||
-      encode_rows_heads_dim(&p.tm_kh, k, rows_k, H, D, bf16, kBN / 2) != ATTN_OK)
-    return ATTN_ERR_CUDA;
-  p.o = o;
-  p.lse = lse;
-  p.cu_q = cu_seqlens_q;
-  p.cu_k = cu_seqlens_k;
+  if ((st = device_state(dev, &ds)) != ATTN_OK) return st;
+  if ((st = host::prepare_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale, cu_seqlens_q,
+                              cu_seqlens_k, dev, call, &p)) != ATTN_OK)
+    return st;
   p.err = ds->err;
-  p.B = B;
-  p.H = H;
-  p.Sq = Sq;
-  p.Sk = Sk;
-  p.varlen = varlen ? 1 : 0;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  p.scale_pos = scale > 0.0f ? 1 : 0;
-  p.timeout_ns = timeout_ns_from_env();
-
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  p.inject = inject_from_env() == 1 ? 1 : 0;
   LaunchInfo info;
-  const cudaError_t e = launch_forward(p, D, bf16, varlen, B, H, rows_q, Sq, ds->sms, s, &info);
+  const cudaError_t e = launch_forward(p, D, call.bf16, call.varlen, B, H, call.rows_q, Sq,
+                                       ds->sms, static_cast<cudaStream_t>(stream), &info);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_CUDA;
@@ -637,7 +545,7 @@ int encode_e4m3_rows(CUtensorMap* m, const void* ptr, long long rows, int H) {
   cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(H) * 128};
   cuuint32_t box[3] = {128, 1, 128};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims,
+  CUresult r = host::encoder_slot()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -649,7 +557,7 @@ int encode_e4m3_vt(CUtensorMap* m, const void* ptr, long long keys, int H) {
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(keys), static_cast<cuuint64_t>(keys) * 128};
   cuuint32_t box[3] = {128, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims,
+  CUresult r = host::encoder_slot()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -729,6 +637,7 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
   q8.o_mul = v_scale;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int grid = static_cast<int>(units < ds->sms ? units : ds->sms);
+  p.pair_blocks = pair_blocks_for(units, grid);
   const uint8_t* v8 = static_cast<const uint8_t*>(v);
   uint8_t* vt = static_cast<uint8_t*>(workspace);
   const cudaError_t e = out_dtype == ATTN_DTYPE_BF16
@@ -804,11 +713,12 @@ extern "C" int attn_release(void) {
   const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
   for (int d = 0; d < kMaxDevices; ++d) {
     DeviceState& s = g_dev[d];
-    if (s.ready && s.err) {
+    if (s.err) {
       if (cudaSetDevice(d) != cudaSuccess || cudaFree(s.err) != cudaSuccess) rc = ATTN_ERR_CUDA;
     }
     s = DeviceState();
   }
+  host::clear_pointer_cache();
   if (have_cur) cudaSetDevice(cur);
   cudaGetLastError();
   return rc;

@@ -615,11 +615,18 @@ __device__ void mma_loop(const BwdParams& p, uint32_t smem, uint32_t tmem, uint3
 }
 
 // ------------------------------------------------------------------- load
+struct BwdLoadLog {
+  FillLog<1> kv;
+  FillLog<2> q, dout;
+};
+
+// Every issued fill is recorded in `f` (see FillLog).
 template <int D, bool VARLEN>
 __device__ void load_loop(const BwdParams& p, uint32_t smem, uint32_t bars, const Ctl& ctl,
-                          uint32_t& g, uint32_t& kv_cnt) {
+                          BwdLoadLog& f) {
   using L = BLayout<D>;
   auto bar = [&](int i) { return bars + 8u * i; };
+  uint32_t g = 0, kv_cnt = 0;
   BUnit w;
   bwd_walk<VARLEN>(p, w, true);
   for (int k = 0; bwd_unit<VARLEN>(p, k, w, true); ++k) {
@@ -632,6 +639,7 @@ __device__ void load_loop(const BwdParams& p, uint32_t smem, uint32_t bars, cons
       ptx::tma_load_3d(smem + L::kKOff + blk * L::kBlk, &p.tm_k, bar(L::KVF), blk * 64, w.h, krow);
       ptx::tma_load_3d(smem + L::kVOff + blk * L::kBlk, &p.tm_v, bar(L::KVF), blk * 64, w.h, krow);
     }
+    f.kv.last[0] = static_cast<int>(kv_cnt);
     ++kv_cnt;
     for (int j = 0; j < w.n; ++j, ++g) {
       const uint32_t st = g & 1u;
@@ -647,6 +655,7 @@ __device__ void load_loop(const BwdParams& p, uint32_t smem, uint32_t bars, cons
       for (int blk = 0; blk < D / 64; ++blk)
         ptx::tma_load_3d(smem + L::kQOff + st * L::kTile + blk * L::kBlk, &p.tm_q,
                          bar(L::QF0 + st), blk * 64, w.h, qrow);
+      f.q.last[st] = static_cast<int>(g);
       // dO tile and D bias
       if (g >= 2 && !wait_bar(bar(L::DOE0 + st), ((g >> 1) - 1) & 1u, ctl)) return;
       ptx::mbar_arrive_expect_tx(bar(L::DOF0 + st), L::kTile + kBiasBytes);
@@ -656,6 +665,7 @@ __device__ void load_loop(const BwdParams& p, uint32_t smem, uint32_t bars, cons
       for (int blk = 0; blk < D / 64; ++blk)
         ptx::tma_load_3d(smem + L::kDoOff + st * L::kDoStage + blk * L::kBlk, &p.tm_do,
                          bar(L::DOF0 + st), blk * 64, w.h, qrow);
+      f.dout.last[st] = static_cast<int>(g);
     }
   }
 }
@@ -720,15 +730,15 @@ __global__ void __maxnreg__(128) attn_bwd_kernel(const __grid_constant__ BwdPara
       wait_bar(done, 0, ctl, false);
     }
   } else if (lane == 0) {
-    uint32_t g = 0, kv_cnt = 0;
-    load_loop<D, VARLEN>(p, smem, bars, ctl, g, kv_cnt);
-    // no TMA write may land after the CTA exits
-    if (kv_cnt > 0) wait_bar(bars + 8u * L::KVF, (kv_cnt - 1) & 1u, ctl, false);
-    for (uint32_t st = 0; st < 2 && st < g; ++st) {
-      const uint32_t last = st + ((g - 1 - st) / 2) * 2;
-      wait_bar(bars + 8u * (L::QF0 + st), (last >> 1) & 1u, ctl, false);
-      wait_bar(bars + 8u * (L::DOF0 + st), (last >> 1) & 1u, ctl, false);
-    }
+    BwdLoadLog f;
+    f.kv.clear();
+    f.q.clear();
+    f.dout.clear();
+    load_loop<D, VARLEN>(p, smem, bars, ctl, f);
+    // no TMA or bulk copy may land after the CTA exits
+    drain_fills(bars, L::KVF, f.kv, ctl);
+    drain_fills(bars, L::QF0, f.q, ctl);
+    drain_fills(bars, L::DOF0, f.dout, ctl);
   }
 
   ptx::tc_fence_before();
@@ -941,7 +951,8 @@ cudaError_t launch_bwd(const BwdParams& p, const uint16_t* o, const uint16_t* do
   // packed sequences walk their bounds; the dense instantiation has no walk
   const void* fn = p.varlen ? reinterpret_cast<const void*>(&attn_bwd_kernel<D, BF16, true>)
                             : reinterpret_cast<const void*>(&attn_bwd_kernel<D, BF16, false>);
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, BLayout<D>::kAlloc);
+  static std::atomic<unsigned long long> opted[2] = {{0}, {0}};
+  e = smem_opt_in(fn, BLayout<D>::kAlloc, opted[p.varlen ? 1 : 0]);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<BwdParams*>(&p)};
   e = cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, BLayout<D>::kAlloc, stream);

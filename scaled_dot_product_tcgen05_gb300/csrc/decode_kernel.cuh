@@ -300,13 +300,18 @@ __device__ void dec_compute(const DecParams& p, uint8_t* base, uint32_t bars, co
 template <int D>
 __device__ void dec_produce(const DecParams& p, uint32_t smem, uint32_t bars, const Ctl& ctl) {
   using L = DLayout<D>;
+  FillLog<kStages> f;
+  f.clear();
   uint32_t it = 0;
+  bool ok = true;
   DUnit w;
-  for (int u = blockIdx.x; dec_unit(p, u, w, true); u += gridDim.x) {
+  for (int u = blockIdx.x; ok && dec_unit(p, u, w, true); u += gridDim.x) {
     for (int j = 0; j < w.ntiles; ++j, ++it) {
       const uint32_t st = it % kStages;
-      if (it >= kStages && !wait_bar(bars + 8u * (L::E + st), (it / kStages - 1) & 1u, ctl))
-        return;
+      if (it >= kStages && !wait_bar(bars + 8u * (L::E + st), (it / kStages - 1) & 1u, ctl)) {
+        ok = false;  // leave both loops; the copies already issued are waited for below
+        break;
+      }
       // injected fault (tests only): this fill never arrives, so the consumers'
       // bounded wait runs out and the call reports ATTN_ERR_DEVICE_TIMEOUT
       if (p.inject == 1 && blockIdx.x == 0 && it == 0) continue;
@@ -320,13 +325,11 @@ __device__ void dec_produce(const DecParams& p, uint32_t smem, uint32_t bars, co
         ptx::tma_load_3d(smem + L::kVOff + st * L::kTile + blk * L::kBlk, &p.tm_v, full,
                          blk * 64, w.h, row);
       }
+      f.last[st] = static_cast<int>(it);
     }
   }
   // no copy may land after the CTA exits: wait for the last fill of each stage
-  for (uint32_t st = 0; st < kStages && st < it; ++st) {
-    const uint32_t last = st + ((it - 1 - st) / kStages) * kStages;
-    wait_bar(bars + 8u * (L::F + st), (last / kStages) & 1u, ctl, false);
-  }
+  drain_fills(bars, L::F, f, ctl);
 }
 
 template <int D, int SQ, bool BF16>
@@ -361,8 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
 template <int D, int SQ, bool BF16>
 cudaError_t launch_decode(const DecParams& p, int grid, cudaStream_t stream) {
   const void* fn = reinterpret_cast<const void*>(&attn_decode_kernel<D, SQ, BF16>);
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       DLayout<D>::kAlloc);
+  static std::atomic<unsigned long long> opted{0};
+  const cudaError_t e = smem_opt_in(fn, DLayout<D>::kAlloc, opted);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<DecParams*>(&p)};
   return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, DLayout<D>::kAlloc, stream);

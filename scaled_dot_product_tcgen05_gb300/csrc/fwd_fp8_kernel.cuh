@@ -188,13 +188,13 @@ __device__ void softmax_role8(const Fp8Params& q8, int t, uint32_t tmem, uint32_
   uint16_t* const O = static_cast<uint16_t*>(p.o);
 
   Cursor cur;
-  init_cursor<kUnitRows>(p, cur, false);
+  init_cursor<kUnitRows, false>(p, cur, false);
   Unit w;
-  for (int k = 0; decode_unit(p, unit_of(k), cur, w, false); ++k) {
+  for (int k = 0; decode_unit<false>(p, slot_unit(p, k), cur, w, false); ++k) {
     if (!(t == 0 ? w.valid[0] : w.valid[1])) continue;
-    const int q0 = w.qt * kUnitRows + t * kBM;
+    const int q0 = w.q0 + t * kBM;
     const int qrow = q0 + row;
-    const bool row_ok = qrow < w.Lq;
+    const bool row_ok = qrow >= 0 && qrow < w.Lq;
     const int n = t == 0 ? w.n[0] : w.n[1];
     const long long orow = (static_cast<long long>(w.q_start) + qrow) * p.H + w.h;
     const long long lidx = (static_cast<long long>(w.b) * p.H + w.h) * p.Sq + qrow;
@@ -256,9 +256,9 @@ static __device__ void mma_loop8(const FwdParams& p, uint32_t smem, uint32_t tme
   const uint64_t dk0 = ptx::desc_sw128(smem + L::kKOff, 16, 1024);
   const uint64_t dv0 = ptx::desc_sw128(smem + L::kVOff, 16, 1024);
   Cursor cur;
-  init_cursor<kUnitRows>(p, cur, false);
+  init_cursor<kUnitRows, false>(p, cur, false);
   Unit w;
-  for (int k = 0; decode_unit(p, unit_of(k), cur, w, false); ++k) {
+  for (int k = 0; decode_unit<false>(p, slot_unit(p, k), cur, w, false); ++k) {
     const int nmax = max(w.n[0], w.n[1]);
     if (nmax == 0) continue;
     if (!wait_bar(bar(L::QF), q_it & 1u, ctl)) return;
@@ -310,15 +310,22 @@ static __device__ void mma_loop8(const FwdParams& p, uint32_t smem, uint32_t tme
 }
 
 // ------------------------------------------------------------------- load
+struct LoadLog8 {
+  FillLog<1> q;
+  FillLog<kStages> k, v;
+};
+
+// Every issued fill is recorded in `f` (see FillLog).
 static __device__ void load_loop8(const Fp8Params& q8, uint32_t smem, uint32_t bars, const Ctl& ctl,
-                           uint32_t& kv_it, uint32_t& q_it) {
+                                  LoadLog8& f) {
   using L = Layout8;
   const FwdParams& p = q8.f;
   auto bar = [&](int i) { return bars + 8u * i; };
+  uint32_t kv_it = 0, q_it = 0;
   Cursor cur;
-  init_cursor<kUnitRows>(p, cur, true);
+  init_cursor<kUnitRows, false>(p, cur, true);
   Unit w;
-  for (int k = 0; decode_unit(p, unit_of(k), cur, w, true); ++k) {
+  for (int k = 0; decode_unit<false>(p, slot_unit(p, k), cur, w, true); ++k) {
     const int nmax = max(w.n[0], w.n[1]);
     if (nmax == 0) continue;
     if (q_it > 0 && !wait_bar(bar(L::QE), (q_it - 1) & 1u, ctl)) return;
@@ -326,7 +333,8 @@ static __device__ void load_loop8(const Fp8Params& q8, uint32_t smem, uint32_t b
 #pragma unroll
     for (int t = 0; t < kTiles; ++t)
       ptx::tma_load_3d(smem + L::kQOff + t * L::kTile, &p.tm_q, bar(L::QF), 0, w.h,
-                       w.q_start + w.qt * kUnitRows + t * kBM);
+                       w.q_start + w.q0 + t * kBM);
+    f.q.last[0] = static_cast<int>(q_it);
     ++q_it;
     for (int j = 0; j < nmax; ++j) {
       const uint32_t it = kv_it + j;
@@ -336,11 +344,13 @@ static __device__ void load_loop8(const Fp8Params& q8, uint32_t smem, uint32_t b
       ptx::mbar_arrive_expect_tx(bar(L::KF + st), L::kTile);
       ptx::tma_load_3d(smem + L::kKOff + st * L::kTile, &p.tm_k, bar(L::KF + st), 0, w.h,
                        w.k_start + kt * kBN);
+      f.k.last[st] = static_cast<int>(it);
       if (it >= kStages && !wait_bar(bar(L::VE + st), (it / kStages - 1) & 1u, ctl)) return;
       ptx::mbar_arrive_expect_tx(bar(L::VF + st), L::kTile);
       // V^T [H, D, B * sk_pad]: x = key (16-byte aligned: sk_pad and 128 kt are), y = dim
       ptx::tma_load_3d(smem + L::kVOff + st * L::kTile, &p.tm_v, bar(L::VF + st),
                        w.b * q8.sk_pad + kt * kBN, 0, w.h);
+      f.v.last[st] = static_cast<int>(it);
     }
     kv_it += nmax;
   }
@@ -389,14 +399,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_fp8_kernel(const __grid_
       wait_bar(done, 0, ctl, false);
     }
   } else if (lane == 0) {
-    uint32_t kv_it = 0, q_it = 0;
-    load_loop8(q8, smem, bars, ctl, kv_it, q_it);
-    if (q_it > 0) wait_bar(bars + 8u * L::QF, (q_it - 1) & 1u, ctl, false);
-    for (uint32_t st = 0; st < kStages && st < kv_it; ++st) {
-      const uint32_t last = st + ((kv_it - 1 - st) / kStages) * kStages;
-      wait_bar(bars + 8u * (L::KF + st), (last / kStages) & 1u, ctl, false);
-      wait_bar(bars + 8u * (L::VF + st), (last / kStages) & 1u, ctl, false);
-    }
+    LoadLog8 f;
+    f.q.clear();
+    f.k.clear();
+    f.v.clear();
+    load_loop8(q8, smem, bars, ctl, f);
+    // no TMA write may land after the CTA exits
+    drain_fills(bars, L::QF, f.q, ctl);
+    drain_fills(bars, L::KF, f.k, ctl);
+    drain_fills(bars, L::VF, f.v, ctl);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -450,7 +461,8 @@ cudaError_t launch_fwd_fp8(const Fp8Params& q8, const uint8_t* v, uint8_t* vt, i
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const void* fn = reinterpret_cast<const void*>(&attn_fwd_fp8_kernel<BF16OUT>);
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout8::kAlloc);
+  static std::atomic<unsigned long long> opted{0};
+  e = smem_opt_in(fn, Layout8::kAlloc, opted);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<Fp8Params*>(&q8)};
   return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, Layout8::kAlloc, stream);

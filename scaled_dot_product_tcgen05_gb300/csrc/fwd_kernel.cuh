@@ -27,6 +27,7 @@
 // device word, tells the other roles through a shared flag and winds down.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -68,6 +69,16 @@ struct FwdParams {
   float scale_log2;          // scale * log2(e)
   int scale_pos;             // scale > 0: fold the scale into the exp2 argument
   long long timeout_ns;      // limit for any single pipeline wait
+  // Schedule items pair the row blocks i and nU-1-i of one (sequence, head)
+  // (see decode_rows); set by the host when the units far outnumber the workers.
+  int pair_blocks = 0;
+  // Offset (from the 1024-aligned origin of the dynamic shared memory) of the
+  // packed-sequence walk order, past every other buffer of the kernel; set by
+  // the host, which adds kOrderBytes to the launch when the order is used.
+  int order_off = 0;
+  // Fault injection for the failure-detection tests (0 in normal use): 1 makes
+  // the loader of CTA 0 skip its first K tile, so a bounded wait runs out.
+  int inject = 0;
 };
 
 template <int D>
@@ -119,6 +130,33 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
   }
 }
 
+// Index of the last copy issued into each buffer of a ring (-1: none).  A
+// loader records every fill when it issues it; after its loop ends, also when
+// it was abandoned half-way through a unit, it waits for exactly the fills
+// that may still be in flight (one per buffer: a buffer is refilled only after
+// its previous fill has landed and been consumed).
+template <int N>
+struct FillLog {
+  int last[N];
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int i = 0; i < N; ++i) last[i] = -1;
+  }
+};
+
+// Bounded waits, ignoring the abort flag, for the last fill of each buffer of
+// a ring whose "full" barriers are full0, full0 + 1, ... (fill i completes
+// phase i / N of barrier i % N).
+template <int N>
+__device__ __forceinline__ void drain_fills(uint32_t bars, int full0, const FillLog<N>& f,
+                                            const Ctl& ctl) {
+#pragma unroll 1
+  for (int st = 0; st < N; ++st)
+    if (f.last[st] >= 0)
+      wait_bar(bars + 8u * (full0 + st), (static_cast<uint32_t>(f.last[st]) / N) & 1u, ctl,
+               false);
+}
+
 // All 32 lanes wait; the warp proceeds only if every lane saw the phase.
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const Ctl& c) {
   const bool ok = wait_bar(bar, parity, c);
@@ -127,7 +165,8 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, con
 
 // ------------------------------------------------------------- work units
 struct Unit {
-  int b, h, qt;               // sequence, head, unit index within the sequence
+  int b, h;                   // sequence, head
+  int q0;                     // first query row of the unit within the sequence (may be < 0)
   int q_start, Lq, k_start, Lk;
   int j0;                     // first K/V tile visited (step j reads tile j0 + j)
   int n[kTiles];              // K/V tiles visited by each query tile
@@ -135,17 +174,69 @@ struct Unit {
 };
 
 struct Cursor {               // forward-only walk over varlen sequences
-  int b, base, units;
+  int b, base, units;         // b: position in the walk order
+  int seq;                    // the sequence at position b
   int q_start, Lq, k_start, Lk;
+  const int* order;           // walk order in shared memory, or null (given order)
 };
+
+// Packed sequences are walked longest first (by Lq * Lk) when there are at
+// most kMaxOrderedSeqs of them, so that the last items dealt to the workers
+// are the cheapest ones and the loads end close together; every CTA ranks the
+// sequences itself at its start (build_seq_order).  Larger batches keep their
+// given order.  The order and the ranking keys live in dynamic shared memory
+// at FwdParams::order_off (static shared memory is avoided: on GB300 even
+// 1 KB of it slowed these kernels by 3-4 %).
+constexpr int kMaxOrderedSeqs = 256;
+constexpr int kOrderBytes = kMaxOrderedSeqs * (4 + 8);
+
+__host__ __device__ __forceinline__ bool seq_ordered(const FwdParams& p) {
+  return p.varlen && p.B <= kMaxOrderedSeqs;
+}
+
+// 1024-aligned origin of the dynamic shared memory (the kernels' layouts start here).
+__device__ __forceinline__ uint8_t* smem_origin() {
+  extern __shared__ uint8_t smem_dyn[];
+  const uint32_t raw = ptx::smem_u32(smem_dyn);
+  return smem_dyn + (((raw + 1023u) & ~1023u) - raw);
+}
+
+// Called by every thread of the CTA before the barrier that ends the kernel's
+// prologue.  Sequence b gets position #{b' : key(b') > key(b), or key(b') ==
+// key(b) and b' < b} (a permutation, also for malformed offsets, which
+// load_seq reports when the walk gets there).  Its own barrier is reached by
+// every launch, ordered or not: a barrier under a condition made the compiler
+// treat the whole kernel's control flow more conservatively (3-6 % slower,
+// measured).
+__device__ __forceinline__ void build_seq_order(const FwdParams& p) {
+  const bool ordered = seq_ordered(p);
+  int* const order = reinterpret_cast<int*>(smem_origin() + p.order_off);
+  long long* const key = reinterpret_cast<long long*>(order + kMaxOrderedSeqs);
+  for (int b = threadIdx.x; ordered && b < p.B; b += blockDim.x) {
+    const long long lq = __ldg(p.cu_q + b + 1) - __ldg(p.cu_q + b);
+    const long long lk = __ldg(p.cu_k + b + 1) - __ldg(p.cu_k + b);
+    key[b] = lq * lk;
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; ordered && b < p.B; b += blockDim.x) {
+    const long long kb = key[b];
+    int r = 0;
+    for (int x = 0; x < p.B; ++x) {
+      const long long kx = key[x];
+      r += (kx > kb || (kx == kb && x < b)) ? 1 : 0;
+    }
+    order[r] = b;
+  }
+}
 
 template <int UR>
 __device__ __forceinline__ void load_seq(const FwdParams& p, Cursor& c, bool report) {
   c.units = 0;
   c.q_start = c.Lq = c.k_start = c.Lk = 0;
   if (c.b >= p.B) return;
-  const int q0 = __ldg(p.cu_q + c.b), q1 = __ldg(p.cu_q + c.b + 1);
-  const int k0 = __ldg(p.cu_k + c.b), k1 = __ldg(p.cu_k + c.b + 1);
+  c.seq = c.order ? c.order[c.b] : c.b;
+  const int q0 = __ldg(p.cu_q + c.seq), q1 = __ldg(p.cu_q + c.seq + 1);
+  const int k0 = __ldg(p.cu_k + c.seq), k1 = __ldg(p.cu_k + c.seq + 1);
   const bool ok = 0 <= q0 && q0 <= q1 && q1 <= p.Sq && 0 <= k0 && k0 <= k1 && k1 <= p.Sk;
   if (!ok) {
     if (report) atomicOr(p.err, kErrBadSeqlens);
@@ -155,32 +246,56 @@ __device__ __forceinline__ void load_seq(const FwdParams& p, Cursor& c, bool rep
   c.Lq = q1 - q0;
   c.k_start = k0;
   c.Lk = k1 - k0;
-  c.units = p.H * ((c.Lq + UR - 1) / UR);
+  const int nU = (c.Lq + UR - 1) / UR;
+  c.units = p.H * (p.pair_blocks ? (nU + 1) / 2 : nU);  // schedule items of this sequence
 }
 
-template <int UR>
+// VL = false compiles the walk for dense batches only (p.varlen must be 0).
+template <int UR, bool VL = true>
 __device__ __forceinline__ void init_cursor(const FwdParams& p, Cursor& c, bool report) {
   c.b = 0;
   c.base = 0;
-  if (p.varlen) load_seq<UR>(p, c, report);
+  c.seq = 0;
+  c.order = VL && seq_ordered(p) ? reinterpret_cast<const int*>(smem_origin() + p.order_off)
+                                  : nullptr;
+  if (VL && p.varlen) load_seq<UR>(p, c, report);
 }
 
-// Decodes unit u (units are visited in increasing order by each CTA) into its
-// sequence, head and row block of UR query rows.
-// Order: (sequence, head) outer, row block inner, heaviest causal blocks
-// first.  Keeping one head's blocks together keeps the K/V tiles that the
-// concurrently running CTAs stream within L2 (one head of a 64K-token
-// sequence is 32 MB); dealing the units to CTAs in a snake order (unit_of)
-// keeps the per-CTA work balanced.
+// Row block `blk` of a sequence, or no rows at all (empty).  Under a causal
+// mask the blocks are aligned to the end of the sequence (block nU-1 ends at
+// the last row), so a partial block holds the first rows, which see the fewest
+// keys; its rows before row 0 are computed as fully masked rows and never
+// written.  Without a causal mask blocks start at row 0.
 template <int UR>
+__device__ __forceinline__ void set_block(const FwdParams& p, Unit& w, int nU, int blk,
+                                          bool empty) {
+  const int off = p.causal ? w.Lq - nU * UR : 0;
+  w.q0 = empty ? w.Lq : off + blk * UR;
+}
+
+// Decodes unit u (units are visited in increasing order by each worker) into
+// its sequence, head and block of UR query rows.
+// Order: (sequence, head) outer, row blocks inner.  Keeping one head's blocks
+// together keeps the K/V tiles that the concurrently running workers stream
+// within L2 (one head of a 64K-token sequence is 32 MB).  Without
+// p.pair_blocks, u enumerates the blocks of a (sequence, head), heaviest
+// causal block first.  With p.pair_blocks, u = 2 s + part: schedule item s
+// holds block nU-1-i (part 0, the heaviest under a causal mask) and block i
+// (part 1) of one (sequence, head), so that every item of a (sequence, head)
+// costs about the same; the middle block of an odd nU stands alone and its
+// part 1 is empty.  Items are dealt to the workers in a snake order (see
+// slot_unit).
+template <int UR, bool VL = true>
 __device__ __forceinline__ bool decode_rows(const FwdParams& p, int u, Cursor& c, Unit& w,
                                             bool report) {
-  if (!p.varlen) {
-    const int nU = (p.Sq + UR - 1) / UR;
-    if (u >= p.B * p.H * nU) return false;
-    const int bh = u / nU;
-    const int i = u - bh * nU;
-    w.qt = p.causal ? (nU - 1 - i) : i;
+  const int s = p.pair_blocks ? (u >> 1) : u;  // schedule item
+  int nU, i;
+  if (!VL || !p.varlen) {
+    nU = (p.Sq + UR - 1) / UR;
+    const int per = p.pair_blocks ? (nU + 1) / 2 : nU;
+    if (s >= p.B * p.H * per) return false;
+    const int bh = s / per;
+    i = s - bh * per;
     w.b = bh / p.H;
     w.h = bh - w.b * p.H;
     w.q_start = w.b * p.Sq;
@@ -190,41 +305,48 @@ __device__ __forceinline__ bool decode_rows(const FwdParams& p, int u, Cursor& c
   } else {
     while (true) {
       if (c.b >= p.B) return false;
-      if (u < c.base + c.units) break;
+      if (s < c.base + c.units) break;
       c.base += c.units;
       c.b += 1;
       load_seq<UR>(p, c, report);
     }
-    const int rem = u - c.base;
-    const int nU = c.units / p.H;
-    w.h = rem / nU;
-    const int i = rem - w.h * nU;
-    w.qt = p.causal ? (nU - 1 - i) : i;
-    w.b = c.b;
+    const int rem = s - c.base;
+    const int per = c.units / p.H;
+    w.h = rem / per;
+    i = rem - w.h * per;
+    nU = (c.Lq + UR - 1) / UR;
+    w.b = c.seq;
     w.q_start = c.q_start;
     w.Lq = c.Lq;
     w.k_start = c.k_start;
     w.Lk = c.Lk;
   }
+  if (p.pair_blocks) {
+    const bool second = (u & 1) != 0;
+    set_block<UR>(p, w, nU, second ? i : nU - 1 - i, second && i == nU - 1 - i);
+  } else {
+    set_block<UR>(p, w, nU, p.causal ? nU - 1 - i : i, false);
+  }
   return true;
 }
 
 // K/V tiles [lo, hi) holding every key that some row of the 128-row query
-// tile starting at row q0 can see (hi <= lo: none).  Tiles outside the range
-// are never loaded or multiplied; keys inside it that a row cannot see are
-// masked in the softmax.
+// tile starting at row q0 (which may be negative: rows before 0 do not exist)
+// can see (hi <= lo: none).  Tiles outside the range are never loaded or
+// multiplied; keys inside it that a row cannot see are masked in the softmax.
 __device__ __forceinline__ void tile_keys(const FwdParams& p, const Unit& w, int q0, int& lo,
                                           int& hi) {
   lo = hi = 0;
-  if (q0 >= w.Lq) return;
+  const int r0 = max(q0, 0);
+  if (r0 >= w.Lq || q0 + kBM <= 0) return;
   const int q1 = min(q0 + kBM, w.Lq) - 1;
   const int nk = (w.Lk + kBN - 1) / kBN;
-  if (q0 < p.global_q) {  // rows that see every key (up to the diagonal when causal)
+  if (r0 < p.global_q) {  // rows that see every key (up to the diagonal when causal)
     hi = p.causal ? min(nk, q1 / kBN + 1) : nk;
     return;
   }
-  // rows q0..q1 see keys q0 - win_left .. q1 + win_right
-  lo = max(0, q0 - p.win_left) / kBN;
+  // rows r0..q1 see keys r0 - win_left .. q1 + win_right
+  lo = max(0, r0 - p.win_left) / kBN;
   hi = static_cast<int>(min(static_cast<long long>(nk),
                             (static_cast<long long>(q1) + p.win_right) / kBN + 1));
 }
@@ -244,19 +366,22 @@ __device__ __forceinline__ void row_keys(const FwdParams& p, const Unit& w, int 
   }
 }
 
+template <bool VL = true>
 __device__ __forceinline__ bool decode_unit(const FwdParams& p, int u, Cursor& c, Unit& w,
                                             bool report) {
-  if (!decode_rows<kUnitRows>(p, u, c, w, report)) return false;
+  if (!decode_rows<kUnitRows, VL>(p, u, c, w, report)) return false;
   int lo[kTiles], hi[kTiles];
+  w.j0 = -1;
 #pragma unroll
   for (int t = 0; t < kTiles; ++t) {
-    const int q0 = w.qt * kUnitRows + t * kBM;
-    w.valid[t] = q0 < w.Lq;
+    const int q0 = w.q0 + t * kBM;
+    w.valid[t] = q0 + kBM > 0 && q0 < w.Lq;
     tile_keys(p, w, q0, lo[t], hi[t]);
+    if (w.j0 < 0 && w.valid[t]) w.j0 = lo[t];
   }
-  // both query tiles walk the K/V tiles from the first one either needs
-  // (tile 0's, the smaller); each stops at its own last tile
-  w.j0 = lo[0];
+  // both query tiles walk the K/V tiles from the first one either needs (that
+  // of the first tile with rows); each stops at its own last tile
+  if (w.j0 < 0) w.j0 = 0;
 #pragma unroll
   for (int t = 0; t < kTiles; ++t) w.n[t] = w.valid[t] ? max(0, hi[t] - w.j0) : 0;
   return true;
@@ -270,6 +395,17 @@ __device__ __forceinline__ int unit_of(int k, int g, int c) {
 }
 __device__ __forceinline__ int unit_of(int k) {
   return unit_of(k, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x));
+}
+
+// The unit of the forward kernels' k-th slot of worker c out of g: with paired
+// blocks, slots 2m and 2m+1 hold the two blocks of the worker's m-th schedule
+// item (items dealt in the snake order of unit_of); otherwise the units
+// themselves are dealt that way.
+__device__ __forceinline__ int slot_unit(const FwdParams& p, int k, int g, int c) {
+  return p.pair_blocks ? 2 * unit_of(k >> 1, g, c) + (k & 1) : unit_of(k, g, c);
+}
+__device__ __forceinline__ int slot_unit(const FwdParams& p, int k) {
+  return slot_unit(p, k, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x));
 }
 
 // ---------------------------------------------------------------- softmax
@@ -426,11 +562,11 @@ __device__ void softmax_role(const FwdParams& p, int t, uint32_t tmem, uint32_t 
   Cursor cur;
   init_cursor<kUnitRows>(p, cur, false);
   Unit w;
-  for (int k = 0; decode_unit(p, unit_of(k), cur, w, false); ++k) {
+  for (int k = 0; decode_unit(p, slot_unit(p, k), cur, w, false); ++k) {
     if (!(t == 0 ? w.valid[0] : w.valid[1])) continue;
-    const int q0 = w.qt * kUnitRows + t * kBM;
+    const int q0 = w.q0 + t * kBM;
     const int qrow = q0 + row;
-    const bool row_ok = qrow < w.Lq;
+    const bool row_ok = qrow >= 0 && qrow < w.Lq;
     const int n = t == 0 ? w.n[0] : w.n[1];
     const long long orow = (static_cast<long long>(w.q_start) + qrow) * p.H + w.h;
     const long long lidx = p.varlen
@@ -505,7 +641,7 @@ __device__ void mma_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint3
   Cursor cur;
   init_cursor<kUnitRows>(p, cur, false);
   Unit w;
-  for (int k = 0; decode_unit(p, unit_of(k), cur, w, false); ++k) {
+  for (int k = 0; decode_unit(p, slot_unit(p, k), cur, w, false); ++k) {
     const int nmax = max(w.n[0], w.n[1]);
     if (nmax == 0) continue;
     if (!wait_bar(bar(L::QF), q_it & 1u, ctl)) return;
@@ -578,15 +714,22 @@ __device__ void mma_role(const FwdParams& p, uint32_t smem, uint32_t tmem, uint3
 
 // ------------------------------------------------------------------- load
 template <int D>
+struct LoadLog {
+  FillLog<1> q;
+  FillLog<Layout<D>::kStages> k, v;
+};
+
+template <int D>
 __device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bars, const Ctl& ctl,
-                          uint32_t& kv_it, uint32_t& q_it) {
+                          LoadLog<D>& f) {
   using L = Layout<D>;
   constexpr int NS = L::kStages;
   auto bar = [&](int i) { return bars + 8u * i; };
+  uint32_t kv_it = 0, q_it = 0;
   Cursor cur;
   init_cursor<kUnitRows>(p, cur, true);
   Unit w;
-  for (int k = 0; decode_unit(p, unit_of(k), cur, w, true); ++k) {
+  for (int k = 0; decode_unit(p, slot_unit(p, k), cur, w, true); ++k) {
     const int nmax = max(w.n[0], w.n[1]);
     if (nmax == 0) continue;
     if (q_it > 0 && !wait_bar(bar(L::QE), (q_it - 1) & 1u, ctl)) return;
@@ -596,24 +739,31 @@ __device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bars, cons
 #pragma unroll
       for (int blk = 0; blk < D / 64; ++blk)
         ptx::tma_load_3d(smem + L::kQOff + t * L::kTileBytes + blk * L::kBlk, &p.tm_q,
-                         bar(L::QF), blk * 64, w.h, w.q_start + w.qt * kUnitRows + t * kBM);
+                         bar(L::QF), blk * 64, w.h, w.q_start + w.q0 + t * kBM);
+    f.q.last[0] = static_cast<int>(q_it);
     ++q_it;
     for (int j = 0; j < nmax; ++j) {
       const uint32_t it = kv_it + j;
       const uint32_t st = it % NS;
       const int krow = w.k_start + (w.j0 + j) * kBN;
       if (it >= NS && !wait_bar(bar(L::KE + st), (it / NS - 1) & 1u, ctl)) return;
-      ptx::mbar_arrive_expect_tx(bar(L::KF + st), L::kTileBytes);
+      // injected fault (tests only): this K tile never arrives, so the MMA
+      // thread's bounded wait runs out and the call reports a device timeout
+      if (!(p.inject == 1 && blockIdx.x == 0 && it == 0)) {
+        ptx::mbar_arrive_expect_tx(bar(L::KF + st), L::kTileBytes);
 #pragma unroll
-      for (int blk = 0; blk < D / 64; ++blk)
-        ptx::tma_load_3d(smem + L::kKOff + st * L::kTileBytes + blk * L::kBlk, &p.tm_k,
-                         bar(L::KF + st), blk * 64, w.h, krow);
+        for (int blk = 0; blk < D / 64; ++blk)
+          ptx::tma_load_3d(smem + L::kKOff + st * L::kTileBytes + blk * L::kBlk, &p.tm_k,
+                           bar(L::KF + st), blk * 64, w.h, krow);
+        f.k.last[st] = static_cast<int>(it);
+      }
       if (it >= NS && !wait_bar(bar(L::VE + st), (it / NS - 1) & 1u, ctl)) return;
       ptx::mbar_arrive_expect_tx(bar(L::VF + st), L::kTileBytes);
 #pragma unroll
       for (int blk = 0; blk < D / 64; ++blk)
         ptx::tma_load_3d(smem + L::kVOff + st * L::kTileBytes + blk * L::kBlk, &p.tm_v,
                          bar(L::VF + st), blk * 64, w.h, krow);
+      f.v.last[st] = static_cast<int>(it);
     }
     kv_it += nmax;
   }
@@ -622,17 +772,16 @@ __device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bars, cons
 template <int D>
 __device__ void load_role(const FwdParams& p, uint32_t smem, uint32_t bars, const Ctl& ctl) {
   using L = Layout<D>;
-  constexpr uint32_t NS = L::kStages;
-  uint32_t kv_it = 0, q_it = 0;
-  load_loop<D>(p, smem, bars, ctl, kv_it, q_it);
-  // Wait for the last copy issued into each buffer so no TMA write can land
-  // after the CTA exits (normally these phases completed long ago).
-  if (q_it > 0) wait_bar(bars + 8u * L::QF, (q_it - 1) & 1u, ctl, false);
-  for (uint32_t st = 0; st < NS && st < kv_it; ++st) {
-    const uint32_t last = st + ((kv_it - 1 - st) / NS) * NS;
-    wait_bar(bars + 8u * (L::KF + st), (last / NS) & 1u, ctl, false);
-    wait_bar(bars + 8u * (L::VF + st), (last / NS) & 1u, ctl, false);
-  }
+  LoadLog<D> f;
+  f.q.clear();
+  f.k.clear();
+  f.v.clear();
+  load_loop<D>(p, smem, bars, ctl, f);
+  // No TMA write may land after the CTA exits: wait for the last copy issued
+  // into each buffer (normally these phases completed long ago).
+  drain_fills(bars, L::QF, f.q, ctl);
+  drain_fills(bars, L::KF, f.k, ctl);
+  drain_fills(bars, L::VF, f.v, ctl);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -655,6 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
+  build_seq_order(p);
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
@@ -684,14 +834,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
+// Opts the kernel `fn` in to `bytes` of dynamic shared memory on the current
+// device, once per device: `done` holds one bit per device for that kernel
+// (setting the attribute on every launch cost host time on every call).
+inline cudaError_t smem_opt_in(const void* fn, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
+// Dynamic shared memory of a launch: the layout, plus the packed-sequence
+// order past its end when that is used (FwdParams::order_off = kBytes).
+template <int D>
+inline int fwd_smem_bytes(const FwdParams& p) {
+  return Layout<D>::kAlloc + (seq_ordered(p) ? kOrderBytes : 0);
+}
+
 template <int D, bool BF16>
-cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_fwd(const FwdParams& params, int grid, cudaStream_t stream) {
+  FwdParams p = params;
+  p.order_off = Layout<D>::kBytes;
   const void* fn = reinterpret_cast<const void*>(&attn_fwd_kernel<D, BF16>);
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Layout<D>::kAlloc);
+  static std::atomic<unsigned long long> opted{0};
+  const cudaError_t e = smem_opt_in(fn, Layout<D>::kAlloc + kOrderBytes, opted);
   if (e != cudaSuccess) return e;
-  void* args[] = {const_cast<FwdParams*>(&p)};
-  return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, Layout<D>::kAlloc, stream);
+  void* args[] = {&p};
+  return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, fwd_smem_bytes<D>(p), stream);
 }
 
 }  // namespace attn

@@ -39,11 +39,13 @@ constexpr int kUR = 2 * kBM;    // query rows per pair unit
 constexpr int kStages = 5;      // K/V ring depth (half tiles: 16 KiB each)
 constexpr int kNBuf = 3;        // S buffers in tensor memory
 constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quarter: column halves 0 and 1
-constexpr int kWarps = kSoftmaxWarps + 3;  // + S-MMA warp, load warp, PV-MMA warp
+constexpr int kEpiWarps = 4;    // one per TMEM lane quarter: O -> global memory
+constexpr int kWarps = kSoftmaxWarps + 3 + kEpiWarps;  // + S-MMA, load, PV-MMA, epilogue
 constexpr int kPairThreads = kWarps * 32;
 constexpr int kPMma = 8;        // issues S = Q K^T; allocates tensor memory
 constexpr int kPLoad = 9;
 constexpr int kPPv = 10;        // issues O += P V
+constexpr int kPEpi = 11;       // first epilogue warp (11..14 cover the four lane quarters)
 
 struct Layout {
   static constexpr int kBlk = 16384;
@@ -57,13 +59,20 @@ struct Layout {
   static constexpr int kBarOff = kVOff + kStages * kVHalf;
   static constexpr int QF = 0, QE = 1, KF = 2, KE = KF + kStages, VF = KE + kStages,
                        VE = VF + kStages, SF = VE + kStages, PF = SF + kNBuf,
-                       PVD = PF + kNBuf, OF = PVD + kNBuf, DONE = OF + 1, kNumBars = DONE + 1;
+                       PVD = PF + kNBuf, OF = PVD + kNBuf, DONE = OF + 1, LDONE = DONE + 1,
+                       LR = LDONE + 1, LF = LR + 1, OFREE = LF + 1, kNumBars = OFREE + 1;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+  // the odd CTA's loader record (last Q fill, last K / V fill per stage),
+  // written into the even CTA before it arrives on LDONE
+  static constexpr int kFillOff = kMiscOff + 16;
+  static constexpr int kFillWords = 1 + 2 * kStages;
   // softmax exchange between the two warps of a row: per-step partial maxima
   // (two step parities x two halves x 128 rows) and the final row sums
-  static constexpr int kXMaxOff = kMiscOff + 16;
+  static constexpr int kXMaxOff = kFillOff + 64;
   static constexpr int kXSumOff = kXMaxOff + 2 * 2 * 128 * 4;
-  static constexpr int kBytes = kXSumOff + 2 * 128 * 2 * 4;
+  // 1 / l of each row of the last finished unit, for the epilogue warps
+  static constexpr int kInvLOff = kXSumOff + 2 * 128 * 2 * 4;
+  static constexpr int kBytes = kInvLOff + 128 * 4;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t kColS = 0, kColO = kNBuf * 128;
   // Per-step barriers come in threes indexed by G % 3; barrier G % 3 completes
@@ -79,16 +88,24 @@ struct Layout {
   //                  giving P(G), which PV(G+2) needs.
   static constexpr uint32_t kPArrivals = 2 * kSoftmaxWarps;  // every softmax warp, both CTAs
   static constexpr uint32_t kDoneArrivals = 2;   // both MMA threads
+  // End of a unit: the softmax warps of column half 0 publish 1 / l (LR, one
+  // arrival per warp); the epilogue warps, having read it, free the slot (LF)
+  // and, having read O out of tensor memory, let the next unit's first
+  // O += P V overwrite it (OFREE, in the even CTA: both CTAs' epilogue warps).
+  static constexpr uint32_t kLrArrivals = kSoftmaxWarps / 2;
+  static constexpr uint32_t kLfArrivals = kEpiWarps;
+  static constexpr uint32_t kOFreeArrivals = 2 * kEpiWarps;
 };
 
 // Same as wait_bar, but with cluster-scope acquire (used where the peer CTA arrives).
-__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, const Ctl& c) {
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, const Ctl& c,
+                                                 bool honor_abort = true) {
   if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = ptx::global_timer_ns();
   for (uint32_t n = 1;; ++n) {
     if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
     if ((n & 15u) == 0) {
-      if (*c.abort_flag) return false;
+      if (honor_abort && *c.abort_flag) return false;
       if (static_cast<long long>(ptx::global_timer_ns() - t0) > c.timeout_ns) {
         *c.abort_flag = 1;
         atomicOr(c.err, kErrTimeout);
@@ -98,7 +115,7 @@ __device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, 
   }
 }
 
-__device__ __forceinline__ int q0_of(const Unit& w, int r) { return w.qt * kUR + r * kBM; }
+__device__ __forceinline__ int q0_of(const Unit& w, int r) { return w.q0 + r * kBM; }
 
 // Decodes the k-th unit of this pair; n = K/V steps of the pair (max over the
 // two CTAs' query tiles).
@@ -106,13 +123,22 @@ __device__ __forceinline__ bool decode_pair(const FwdParams& p, int k, Cursor& c
                                             int& n, bool report) {
   const int g = static_cast<int>(gridDim.x) / 2;
   const int cl = static_cast<int>(blockIdx.x) / 2;
-  if (!decode_rows<kUR>(p, unit_of(k, g, cl), c, w, report)) return false;
+  if (!decode_rows<kUR>(p, slot_unit(p, k, g, cl), c, w, report)) return false;
   int lo0, hi0, lo1, hi1;
   tile_keys(p, w, q0_of(w, 0), lo0, hi0);
   tile_keys(p, w, q0_of(w, 1), lo1, hi1);
-  // the pair shares every K/V tile: from the even CTA's first to the last either needs
-  w.j0 = lo0;
-  n = max(0, max(hi0, hi1) - lo0);
+  // the pair shares every K/V tile: from the first to the last that either CTA's rows need
+  int j0 = 0x7fffffff, j1 = 0;
+  if (hi0 > lo0) {
+    j0 = lo0;
+    j1 = hi0;
+  }
+  if (hi1 > lo1) {
+    j0 = min(j0, lo1);
+    j1 = max(j1, hi1);
+  }
+  w.j0 = j1 > 0 ? j0 : 0;
+  n = max(0, j1 - w.j0);
   return true;
 }
 
@@ -124,7 +150,8 @@ __device__ __forceinline__ bool decode_pair(const FwdParams& p, int k, Cursor& c
 // barrier, so both take the same running max and rescale decisions; each
 // writes its 32 columns of P and rescales its 64 columns of O.  Masking: keys
 // c of this half with c < lo or c > limit are invisible (both already local to
-// the half).
+// the half).  Returns false if the wait before a rescale of O gave up (after
+// the step's named barrier).
 template <bool BF16>
 __device__ __forceinline__ bool softmax_half_step(uint32_t tS, uint32_t tP, uint32_t tO, int lo,
                                                   int limit,
@@ -199,7 +226,10 @@ __device__ __forceinline__ bool softmax_half_step(uint32_t tS, uint32_t tP, uint
   st.l_p = st.l_p * alpha + (sum + (round16<BF16>(p_big) - p_big));
 
   if (!first && __any_sync(0xffffffffu, rescale)) {
-    if (!wait_bar_warp(pvd_bar, pvd_parity, ctl)) return false;
+    if (!wait_bar_warp(pvd_bar, pvd_parity, ctl)) {
+      ptx::tmem_wait_st();  // no tensor-memory store of this warp left in flight
+      return false;
+    }
     ptx::tc_fence_after();
     const uint64_t al2 = ptx::f2(alpha, alpha);
 #pragma unroll
@@ -221,6 +251,20 @@ __device__ __forceinline__ bool softmax_half_step(uint32_t tS, uint32_t tP, uint
   return true;
 }
 
+// After a wait of a softmax warp gave up: the warp's remaining arrivals at its
+// named barrier -- `pending` of the current unit k, then n + 1 for every later
+// unit with n steps (one per step and the closing exchange of the row sums).
+// The two warps of a row walk the same units and steps, so the partner warp,
+// which may have passed the same wait, never stays at that barrier.
+static __device__ __noinline__ void finish_row_barriers(const FwdParams& p, Cursor cur, int k,
+                                                        int pending, uint32_t xbar) {
+  for (int i = 0; i < pending; ++i) ptx::named_bar_sync(xbar, 64);
+  Unit w;
+  int n = 0;
+  for (++k; decode_pair(p, k, cur, w, n, false); ++k)
+    for (int i = 0; n > 0 && i <= n; ++i) ptx::named_bar_sync(xbar, 64);
+}
+
 template <bool BF16>
 __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, uint32_t bars,
                              uint8_t* base, const Ctl& ctl) {
@@ -233,23 +277,20 @@ __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, u
   const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t tO = tmem + lane_bits + L::kColO + half * 64;
   const uint32_t bar_p_lead = ptx::mapa(bars + 8 * L::PF, 0);  // + 8 * (G % 3)
-  const uint32_t bar_o = bars + 8 * L::OF;
+  const uint32_t bar_lr = bars + 8 * L::LR, bar_lf = bars + 8 * L::LF;
   const uint32_t xbar = 1 + quarter;  // named barrier of the two warps of these rows
   float* const xmax = reinterpret_cast<float*>(base + L::kXMaxOff);  // [parity][half][row]
   float* const xsum = reinterpret_cast<float*>(base + L::kXSumOff);  // [half][row][2]
-  uint32_t o_cnt = 0, g_base = 0;
-  uint16_t* const O = static_cast<uint16_t*>(p.o);
+  float* const inv_l_slot = reinterpret_cast<float*>(base + L::kInvLOff);
+  uint32_t lr_cnt = 0, g_base = 0;
 
   Cursor cur;
   init_cursor<kUR>(p, cur, false);
   Unit w;
   int n = 0;
   for (int k = 0; decode_pair(p, k, cur, w, n, false); ++k) {
-    const int q0 = q0_of(w, static_cast<int>(rank));
-    if (q0 >= w.Lq && n == 0) continue;
-    const int qrow = q0 + row;
-    const bool row_ok = qrow < w.Lq;
-    const long long orow = (static_cast<long long>(w.q_start) + qrow) * p.H + w.h;
+    const int qrow = q0_of(w, static_cast<int>(rank)) + row;
+    const bool row_ok = qrow >= 0 && qrow < w.Lq;
     const long long lidx = p.varlen
                                ? static_cast<long long>(w.h) * p.Sq + w.q_start + qrow
                                : (static_cast<long long>(w.b) * p.H + w.h) * p.Sq + qrow;
@@ -262,7 +303,10 @@ __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, u
       for (int j = 0, kb = w.j0 * kBN; j < n; ++j, kb += kBN) {
         const uint32_t G = g_base + j;
         const uint32_t b = G % kNBuf;
-        if (!wait_bar_warp(bars + 8 * (L::SF + b), (G / kNBuf) & 1u, ctl)) return;
+        if (!wait_bar_warp(bars + 8 * (L::SF + b), (G / kNBuf) & 1u, ctl)) {
+          finish_row_barriers(p, cur, k, n - j + 1, xbar);
+          return;
+        }
         ptx::tc_fence_after();
         const int lo = key_lo - kb;
         const int limit = min(63, key_hi - kb);
@@ -273,8 +317,10 @@ __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, u
         if (!softmax_half_step<BF16>(tSb + 64 * half, tSb + 32 * half, tO, lo, limit, p.scale_log2,
                                      p.scale_pos != 0, j == 0, rs, xm + half * 128 + row,
                                      xm + (1 - half) * 128 + row, xbar,
-                                     bars + 8 * (L::PVD + gp % kNBuf), (gp / kNBuf) & 1u, ctl))
+                                     bars + 8 * (L::PVD + gp % kNBuf), (gp / kNBuf) & 1u, ctl)) {
+          finish_row_barriers(p, cur, k, n - j, xbar);
           return;
+        }
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive_cluster_relaxed(bar_p_lead + 8u * b);
@@ -286,34 +332,86 @@ __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, u
       ptx::named_bar_sync(xbar, 64);
       rs.l_p += xsum[((1 - half) * 128 + row) * 2 + 0];
       rs.l_x += xsum[((1 - half) * 128 + row) * 2 + 1];
-      if (!wait_bar_warp(bar_o, o_cnt & 1u, ctl)) return;
-      ++o_cnt;
-      ptx::tc_fence_after();
-      const float inv_l = rs.l_p > 0.0f ? 1.0f / rs.l_p : 0.0f;
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t o[32];
-        ptx::tmem_ld_x32(tO + c0, o);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = ptx::pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
-                                   __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(O + orow * D + half * 64 + c0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      if (half == 0) {  // hand 1 / l to the epilogue warps once they have read the last one
+        if (lr_cnt > 0 && !wait_bar_warp(bar_lf, (lr_cnt - 1) & 1u, ctl)) {
+          finish_row_barriers(p, cur, k, 0, xbar);
+          return;
         }
+        inv_l_slot[row] = rs.l_p > 0.0f ? 1.0f / rs.l_p : 0.0f;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_lr);
+        ++lr_cnt;
       }
-    } else if (row_ok) {  // no visible key at all: O = 0, LSE = -inf
-      uint4* dst = reinterpret_cast<uint4*>(O + orow * D + half * 64);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
     }
+    // rows without any visible key (n = 0) get LSE = -inf; their O = 0 is
+    // written by the epilogue warps
     if (row_ok && half == 0) {
       p.lse[lidx] = rs.l_x > 0.0f ? (rs.m + ptx::lg2(rs.l_x)) * 0.69314718055994531f : -INFINITY;
     }
+  }
+}
+
+// Epilogue warps (one per TMEM lane quarter, thread = query row): per unit,
+// wait for 1 / l and for the unit's last O += P V, read O (all 128 columns)
+// out of tensor memory, release it to the next unit's products, then scale,
+// round and store the row.  The softmax warps meanwhile start the next unit.
+template <bool BF16>
+__device__ void epilogue_role(const FwdParams& p, uint32_t rank, uint32_t tmem, uint32_t bars,
+                              uint8_t* base, const Ctl& ctl) {
+  using L = Layout;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+  const int row = quarter * 32 + lane;
+  const uint32_t tO = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + L::kColO;
+  const uint32_t bar_lr = bars + 8 * L::LR, bar_lf = bars + 8 * L::LF, bar_of = bars + 8 * L::OF;
+  const uint32_t bar_free_lead = ptx::mapa(bars + 8 * L::OFREE, 0);
+  const float* const inv_l_slot = reinterpret_cast<const float*>(base + L::kInvLOff);
+  uint16_t* const O = static_cast<uint16_t*>(p.o);
+  uint32_t cnt = 0;
+
+  Cursor cur;
+  init_cursor<kUR>(p, cur, false);
+  Unit w;
+  int n = 0;
+  for (int k = 0; decode_pair(p, k, cur, w, n, false); ++k) {
+    const int qrow = q0_of(w, static_cast<int>(rank)) + row;
+    const bool row_ok = qrow >= 0 && qrow < w.Lq;
+    const long long orow = (static_cast<long long>(w.q_start) + qrow) * p.H + w.h;
+    if (n == 0) {  // no visible key: O = 0
+      if (row_ok) {
+        uint4* const dst = reinterpret_cast<uint4*>(O + orow * D);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      continue;
+    }
+    if (!wait_bar_warp(bar_lr, cnt & 1u, ctl)) return;
+    const float inv_l = inv_l_slot[row];
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar_lf);
+    if (!wait_bar_warp(bar_of, cnt & 1u, ctl)) return;
+    ++cnt;
+    ptx::tc_fence_after();
+    uint4* const dst = reinterpret_cast<uint4*>(O + (row_ok ? orow : 0) * D);
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 64) {
+      uint32_t o[64];
+      ptx::tmem_ld_x64(tO + c0, o);
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        pk[i] = ptx::pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
+                                 __uint_as_float(o[2 * i + 1]) * inv_l);
+      if (row_ok)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          dst[c0 / 8 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
+    // every load of O has completed (tcgen05.ld waits): the next unit may overwrite it
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive_cluster_relaxed(bar_free_lead);
   }
 }
 
@@ -376,6 +474,7 @@ __device__ void pv_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint32
   uint32_t g_base = 0;
   const uint64_t dv0 = ptx::desc_sw128(smem + L::kVOff, L::kBlk, 1024);
   const uint32_t tO = tmem + L::kColO;
+  uint32_t u_cnt = 0;  // units with steps so far
   Cursor cur;
   init_cursor<kUR>(p, cur, false);
   Unit w;
@@ -386,6 +485,10 @@ __device__ void pv_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint32
       const uint32_t G = g_base + j;
       // O += P(G) V(G): P(G) in buffer G % 3 of both CTAs
       if (!wait_bar_cluster(bar(L::PF + G % kNBuf), (G / kNBuf) & 1u, ctl)) return;
+      // the unit's first product overwrites O: the previous unit's O must have been read
+      if (j == 0 && u_cnt > 0 &&
+          !wait_bar_cluster(bar(L::OFREE), (u_cnt - 1) & 1u, ctl))
+        return;
       const uint32_t st = G % NS;
       if (!wait_bar(bar(L::VF + st), (G / NS) & 1u, ctl)) return;
       ptx::tc_fence_after();
@@ -400,6 +503,7 @@ __device__ void pv_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint32
       if (j == n - 1) ptx::mma_commit_pair(bar(L::OF), kBoth);
     }
     g_base += n;
+    ++u_cnt;
   }
 }
 
@@ -412,15 +516,23 @@ __device__ __forceinline__ void mma_drain(uint32_t bars, const Ctl& ctl) {
 }
 
 // ------------------------------------------------------------------- load
+struct PairLoadLog {
+  FillLog<1> q;
+  FillLog<kStages> k, v;
+};
+
 // Runs on lane 0 of the load warp of both CTAs; each loads its own Q tile and
-// its half of every K/V tile, counting the bytes on the even CTA's barriers.
+// its half of every K/V tile, counting the bytes on the even CTA's barriers
+// (the even CTA arms each phase for both halves).  Every issued fill is
+// recorded in `f`.
 static __device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bars, uint32_t rank,
-                                 const Ctl& ctl, uint32_t& kv_it, uint32_t& q_it) {
+                                 const Ctl& ctl, PairLoadLog& f) {
   using L = Layout;
   constexpr int NS = kStages;
   const bool lead = rank == 0;
   auto bar = [&](int i) { return bars + 8u * i; };
   auto lbar = [&](int i) { return ptx::mapa(bars + 8u * i, 0); };
+  uint32_t kv_it = 0, q_it = 0;
   Cursor cur;
   init_cursor<kUR>(p, cur, true);
   Unit w;
@@ -433,39 +545,92 @@ static __device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bar
     for (int blk = 0; blk < D / 64; ++blk)
       ptx::tma_load_3d_pair(smem + L::kQOff + blk * L::kBlk, &p.tm_q, lbar(L::QF), blk * 64, w.h,
                             w.q_start + q0_of(w, static_cast<int>(rank)));
+    f.q.last[0] = static_cast<int>(q_it);
     ++q_it;
     for (int j = 0; j < n; ++j) {
       const uint32_t it = kv_it + j;
       const uint32_t st = it % NS;
       const int krow = w.k_start + (w.j0 + j) * kBN;
       if (it >= NS && !wait_bar(bar(L::KE + st), (it / NS - 1) & 1u, ctl)) return;
-      if (lead) ptx::mbar_arrive_expect_tx(bar(L::KF + st), 2 * L::kKHalf);
+      // injected fault (tests only): the even CTA of pair 0 neither arms nor
+      // loads its first K half, so the S thread's bounded wait runs out
+      if (!(p.inject == 1 && lead && blockIdx.x == 0 && it == 0)) {
+        if (lead) ptx::mbar_arrive_expect_tx(bar(L::KF + st), 2 * L::kKHalf);
 #pragma unroll
-      for (int blk = 0; blk < D / 64; ++blk)
-        ptx::tma_load_3d_pair(smem + L::kKOff + st * L::kKHalf + blk * L::kKBlk, &p.tm_kh,
-                              lbar(L::KF + st), blk * 64, w.h, krow + 64 * static_cast<int>(rank));
+        for (int blk = 0; blk < D / 64; ++blk)
+          ptx::tma_load_3d_pair(smem + L::kKOff + st * L::kKHalf + blk * L::kKBlk, &p.tm_kh,
+                                lbar(L::KF + st), blk * 64, w.h,
+                                krow + 64 * static_cast<int>(rank));
+        f.k.last[st] = static_cast<int>(it);
+      }
       if (it >= NS && !wait_bar(bar(L::VE + st), (it / NS - 1) & 1u, ctl)) return;
       if (lead) ptx::mbar_arrive_expect_tx(bar(L::VF + st), 2 * L::kVHalf);
       ptx::tma_load_3d_pair(smem + L::kVOff + st * L::kVHalf, &p.tm_v, lbar(L::VF + st),
                             64 * static_cast<int>(rank), w.h, krow);
+      f.v.last[st] = static_cast<int>(it);
     }
     kv_it += n;
   }
 }
 
-static __device__ void load_role(const FwdParams& p, uint32_t smem, uint32_t bars, uint32_t rank,
-                                 const Ctl& ctl) {
+// Settles the open phase of one "full" barrier of the even CTA after both
+// loaders have stopped and waits (bounded) for it.  `mine` / `peer` are the
+// last fills the even / odd CTA issued into this buffer: only the later one
+// can still be open (a buffer is refilled only after its previous fill
+// completed).  A fill the even CTA issued was armed for both halves; if the
+// odd CTA never sent its half, those bytes are counted here.  A fill only the
+// odd CTA issued was never armed; it is armed here for the odd half alone.
+__device__ __forceinline__ void settle_fill(uint32_t bar, int mine, int peer, int ring,
+                                            uint32_t half_bytes, const Ctl& ctl) {
+  const int last = max(mine, peer);
+  if (last < 0) return;
+  if (mine < last)
+    ptx::mbar_arrive_expect_tx(bar, half_bytes);
+  else if (peer < last)
+    ptx::mbar_complete_tx(bar, half_bytes);
+  wait_bar(bar, (static_cast<uint32_t>(last) / ring) & 1u, ctl, false);
+}
+
+static __device__ void load_role(const FwdParams& p, uint32_t smem, uint8_t* base, uint32_t bars,
+                                 uint32_t rank, const Ctl& ctl) {
   using L = Layout;
-  uint32_t kv_it = 0, q_it = 0;
-  load_loop(p, smem, bars, rank, ctl, kv_it, q_it);
-  if (rank != 0) return;
-  // The even CTA's "full" barriers count both CTAs' copies: waiting for the
-  // last phase of each means no copy of the pair is still in flight.
-  if (q_it > 0) wait_bar(bars + 8u * L::QF, (q_it - 1) & 1u, ctl, false);
-  for (uint32_t st = 0; st < static_cast<uint32_t>(kStages) && st < kv_it; ++st) {
-    const uint32_t last = st + ((kv_it - 1 - st) / kStages) * kStages;
-    wait_bar(bars + 8u * (L::KF + st), (last / kStages) & 1u, ctl, false);
-    wait_bar(bars + 8u * (L::VF + st), (last / kStages) & 1u, ctl, false);
+  PairLoadLog f;
+  f.q.clear();
+  f.k.clear();
+  f.v.clear();
+  load_loop(p, smem, bars, rank, ctl, f);
+  const uint32_t rec = smem + L::kFillOff;
+  if (rank != 0) {
+    // hand this CTA's record to the even CTA, whose barriers count our copies
+    const uint32_t dst = ptx::mapa(rec, 0);
+    ptx::st_shared_cluster(dst, static_cast<uint32_t>(f.q.last[0]));
+#pragma unroll
+    for (int st = 0; st < kStages; ++st) {
+      ptx::st_shared_cluster(dst + 4u * (1 + st), static_cast<uint32_t>(f.k.last[st]));
+      ptx::st_shared_cluster(dst + 4u * (1 + kStages + st), static_cast<uint32_t>(f.v.last[st]));
+    }
+    ptx::mbar_arrive_cluster(ptx::mapa(bars + 8u * L::LDONE, 0));  // release: stores first
+    return;
+  }
+  // Even CTA: no copy of the pair may land after either CTA exits (the odd one
+  // leaves only after the closing cluster barrier, which this thread reaches
+  // after the waits below).
+  PairLoadLog o = f;
+  if (wait_bar_cluster(bars + 8u * L::LDONE, 0, Ctl{ctl.abort_flag, ctl.err, ctl.timeout_ns},
+                       false)) {
+    const int* r = reinterpret_cast<const int*>(base + L::kFillOff);
+    o.q.last[0] = r[0];
+#pragma unroll
+    for (int st = 0; st < kStages; ++st) {
+      o.k.last[st] = r[1 + st];
+      o.v.last[st] = r[1 + kStages + st];
+    }
+  }
+  settle_fill(bars + 8u * L::QF, f.q.last[0], o.q.last[0], 1, L::kQTile, ctl);
+#pragma unroll 1
+  for (int st = 0; st < kStages; ++st) {
+    settle_fill(bars + 8u * (L::KF + st), f.k.last[st], o.k.last[st], kStages, L::kKHalf, ctl);
+    settle_fill(bars + 8u * (L::VF + st), f.v.last[st], o.v.last[st], kStages, L::kVHalf, ctl);
   }
 }
 
@@ -489,11 +654,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     for (int i = 0; i < L::kNumBars; ++i)
       ptx::mbar_init(bars + 8u * i, (i >= L::PF && i < L::PF + kNBuf) ? L::kPArrivals
                                     : i == L::DONE                  ? L::kDoneArrivals
+                                    : i == L::LR                    ? L::kLrArrivals
+                                    : i == L::LF                    ? L::kLfArrivals
+                                    : i == L::OFREE                 ? L::kOFreeArrivals
                                                                     : 1u);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
   ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA use
+  build_seq_order(p);
   if (warp == kPMma) {
     ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), kTmemCols);
     ptx::tmem_relinquish_pair();
@@ -521,8 +690,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       pv_loop<BF16>(p, smem, tmem, bars, ctl);
       mma_drain(bars, ctl);
     }
-  } else if (lane == 0) {
-    load_role(p, smem, bars, rank, ctl);
+  } else if (warp == kPLoad) {
+    if (lane == 0) load_role(p, smem, base, bars, rank, ctl);
+  } else {
+    epilogue_role<BF16>(p, rank, tmem, bars, base, ctl);
   }
 
   ptx::tc_fence_before();
@@ -532,14 +703,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   if (warp == kPMma) ptx::tmem_dealloc_pair(tmem, kTmemCols);
 }
 
+inline int fwd_2sm_smem_bytes(const FwdParams& p) {
+  return Layout::kAlloc + (seq_ordered(p) ? kOrderBytes : 0);
+}
+
 template <bool BF16>
-cudaError_t launch_fwd_2sm(const FwdParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_fwd_2sm(const FwdParams& params, int grid, cudaStream_t stream) {
+  FwdParams p = params;
+  p.order_off = Layout::kBytes;  // the packed-sequence order follows the layout
   const void* fn = reinterpret_cast<const void*>(&attn_fwd_kernel_2sm<BF16>);
-  cudaError_t e =
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout::kAlloc);
+  static std::atomic<unsigned long long> opted{0};
+  const cudaError_t e = smem_opt_in(fn, Layout::kAlloc + kOrderBytes, opted);
   if (e != cudaSuccess) return e;
-  void* args[] = {const_cast<FwdParams*>(&p)};
-  return cudaLaunchKernel(fn, dim3(grid), dim3(kPairThreads), args, Layout::kAlloc, stream);
+  void* args[] = {&p};
+  return cudaLaunchKernel(fn, dim3(grid), dim3(kPairThreads), args, fwd_2sm_smem_bytes(p),
+                          stream);
 }
 
 }  // namespace pair

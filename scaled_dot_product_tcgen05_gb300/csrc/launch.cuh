@@ -47,19 +47,28 @@ inline long long units_bound(bool varlen, int B, int H, long long rows_q, int Sq
                 : static_cast<long long>(B) * H * ((Sq + rows_per_unit - 1) / rows_per_unit);
 }
 
+// Paired row blocks (FwdParams::pair_blocks) balance the workers' loads when
+// each worker gets many units; with few units per worker they would only halve
+// the parallelism.
+inline int pair_blocks_for(long long units, long long workers) {
+  return units >= 16 * workers ? 1 : 0;
+}
+
 // Head dim 128 runs on CTA pairs with 2-SM MMAs; head dim 64 on single CTAs.
 // ATTN_PAIR=0 sends head dim 128 to the single-CTA kernel as well (kept for
 // cross-checks).  The grid is persistent: at most one CTA per SM.
-inline cudaError_t launch_forward(const FwdParams& p, int D, bool bf16, bool varlen, int B, int H,
-                                  long long rows_q, int Sq, int sms, cudaStream_t s,
+inline cudaError_t launch_forward(const FwdParams& params, int D, bool bf16, bool varlen, int B,
+                                  int H, long long rows_q, int Sq, int sms, cudaStream_t s,
                                   LaunchInfo* info) {
+  FwdParams p = params;
   const char* sel = std::getenv("ATTN_PAIR");
   const bool use_pair = D == 128 && sms >= 2 && !(sel != nullptr && sel[0] == '0');
   if (use_pair) {
     const long long units = units_bound(varlen, B, H, rows_q, Sq, pair::kUR);
     const long long pairs = units < sms / 2 ? units : sms / 2;
+    p.pair_blocks = pair_blocks_for(units, pairs);
     info->grid = static_cast<int>(2 * pairs);
-    info->smem = pair::Layout::kAlloc;
+    info->smem = pair::fwd_2sm_smem_bytes(p);
     info->pair = true;
     if (pairs <= 0) return cudaSuccess;
     return bf16 ? pair::launch_fwd_2sm<true>(p, info->grid, s)
@@ -68,12 +77,13 @@ inline cudaError_t launch_forward(const FwdParams& p, int D, bool bf16, bool var
   const long long units = units_bound(varlen, B, H, rows_q, Sq, kUnitRows);
   info->grid = static_cast<int>(units < sms ? units : sms);
   info->pair = false;
+  p.pair_blocks = pair_blocks_for(units, info->grid);
   if (D == 64) {
-    info->smem = Layout<64>::kAlloc;
+    info->smem = fwd_smem_bytes<64>(p);
     if (info->grid <= 0) return cudaSuccess;
     return bf16 ? launch_fwd<64, true>(p, info->grid, s) : launch_fwd<64, false>(p, info->grid, s);
   }
-  info->smem = Layout<128>::kAlloc;
+  info->smem = fwd_smem_bytes<128>(p);
   if (info->grid <= 0) return cudaSuccess;
   return bf16 ? launch_fwd<128, true>(p, info->grid, s) : launch_fwd<128, false>(p, info->grid, s);
 }

@@ -22,6 +22,8 @@
 
 #include <cstdint>
 
+#include "fwd_kernel.cuh"
+
 namespace attn {
 namespace dec {
 
@@ -97,8 +99,9 @@ cudaError_t launch_merge(const Tin* o_parts, const float* lse_parts, int P, int 
   if (rows == 0) return cudaSuccess;
   const size_t smem = static_cast<size_t>(kMergeWarps) * D * sizeof(float);
   const void* fn = reinterpret_cast<const void*>(&attn_merge_kernel<Tin, BF16>);
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  static std::atomic<unsigned long long> opted{0};  // opted in for the largest head dim
+  cudaError_t e = smem_opt_in(fn, kMergeWarps * kMergeMaxD * static_cast<int>(sizeof(float)),
+                              opted);
   if (e != cudaSuccess) return e;
   attn_merge_kernel<Tin, BF16><<<static_cast<unsigned>(rows), kMergeWarps * 32, smem, stream>>>(
       o_parts, lse_parts, P, B, S, H, D, o, lse);

@@ -180,6 +180,17 @@ __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
+// Counts `bytes` as arrived on the current phase of a local mbarrier without an
+// arrival (used to settle a phase whose expected peer copy was never issued).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+// 32-bit store into shared memory of a CTA of the cluster (cluster address).
+__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
 // Poll with acquire at cluster scope (arrivals come from the peer CTA too).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;

@@ -3,10 +3,16 @@
 Every device-side wait is bounded (ATTN_WAIT_TIMEOUT_MS); when one runs out the
 kernel writes the error word, its roles drain and the CTA exits, so the
 context stays usable and attn_check reports ATTN_ERR_DEVICE_TIMEOUT.  The
-injected faults (ATTN_INJECT_FAULT, honoured by attn_fwd_decode only) are a
-tile fill that is never issued (1: a wait runs out) and an empty launch grid
-that the launch itself rejects (2: ATTN_ERR_CUDA).  Neither traps, faults or
-hangs the GPU.  Host-side failures (no device, bad arguments) are covered
+injected faults (ATTN_INJECT_FAULT) are a tile fill that is never issued (1:
+block 0 of the forward kernels -- the CTA-pair kernel for head dim 128 and the
+single-CTA kernel for head dim 64 -- skips its first K tile, block 0 of the
+decode kernel its first fill, so a wait runs out) and an empty launch grid that
+the launch itself rejects (2, decode only: ATTN_ERR_CUDA).  Neither traps,
+faults or hangs the GPU.  The forward cases run units with more K/V tiles than
+the loaders have stages, so a loader gives up in the middle of a unit and must
+drain exactly the copies it issued; in the CTA-pair kernel the two softmax
+warps of a row may give up at different points and must still meet at their
+shared barrier.  Host-side failures (no device, bad arguments) are covered
 without a GPU.
 """
 import ctypes
@@ -18,8 +24,8 @@ import pytest
 import torch
 
 import scaled_dot_product_tcgen05_gb300 as pkg
-from oracle.sdpa_oracle import attention_decode
-from parity_helpers import compare
+from oracle.sdpa_oracle import attention_decode, attention_dense
+from parity_helpers import compare, run_gpu
 
 
 class _env:
@@ -71,6 +77,16 @@ def _decode_case():
     return q, k, v
 
 
+def _long_decode_case():
+    """One query against a 65536-row cache: block 0 streams 8 fills through 4 stages."""
+    g = torch.Generator().manual_seed(46)
+    B, Sq, Sk, H, D = 1, 1, 65536, 1, 128
+    q = torch.randn(B, Sq, H, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, Sk, H, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, Sk, H, D, generator=g).to(torch.bfloat16)
+    return q, k, v
+
+
 def _run_decode(q, k, v):
     dev = "cuda:0"
     o, lse = pkg.attn_decode(q.to(dev), k.to(dev), v.to(dev), causal=True,
@@ -79,10 +95,12 @@ def _run_decode(q, k, v):
 
 
 @pytest.mark.gpu
-def test_bounded_wait_runs_out_and_the_context_stays_usable():
+@pytest.mark.parametrize("case", [_decode_case, _long_decode_case],
+                         ids=["one_fill_per_block", "more_fills_than_stages"])
+def test_bounded_wait_runs_out_and_the_context_stays_usable(case):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    q, k, v = _decode_case()
+    q, k, v = case()
     with _env(ATTN_INJECT_FAULT=1, ATTN_WAIT_TIMEOUT_MS=200):
         _, _, st = _run_decode(q, k, v)
     assert st == pkg.ATTN_ERR_DEVICE_TIMEOUT, pkg.status_string(st)
@@ -122,3 +140,26 @@ def test_debug_log_names_each_launch(capfd):
     err = capfd.readouterr().err
     grid, smem = pkg.last_launch()
     assert f"attn: attn_fwd_decode grid={grid} smem={smem}" in err, err
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D", [128, 64], ids=["cta_pair_kernel", "single_cta_kernel"])
+def test_forward_bounded_wait_runs_out_and_the_context_stays_usable(D):
+    """attn_fwd with a K tile that never arrives: every role of the affected CTAs winds
+    down within the time limit, the call reports ATTN_ERR_DEVICE_TIMEOUT, and the same
+    call without the fault then matches the oracle on the same context.  S = 1000 gives
+    the first unit of pair / block 0 eight K/V tiles, more than either ring holds."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    g = torch.Generator().manual_seed(47 + D)
+    B, S, H = 1, 1000, 4
+    q, k, v = (torch.randn(B, S, H, D, generator=g).to(torch.bfloat16) for _ in range(3))
+    scale = 1 / math.sqrt(D)
+    dev = "cuda:0"
+    with _env(ATTN_INJECT_FAULT=1, ATTN_WAIT_TIMEOUT_MS=200):
+        pkg.attn_fwd(q.to(dev), k.to(dev), v.to(dev), causal=True, scale=scale)
+        st = pkg.attn_check()
+    assert st == pkg.ATTN_ERR_DEVICE_TIMEOUT, pkg.status_string(st)
+    o, lse = run_gpu(q, k, v, True, scale)  # asserts ATTN_OK
+    o_ref, l_ref = attention_dense(q, k, v, scale, True)
+    compare(o, lse, o_ref, l_ref, what=f"forward D={D} after an injected timeout")

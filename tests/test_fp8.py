@@ -104,3 +104,26 @@ def test_fp8_full_size_sampled_rows():
     l_s = lse[:, heads][:, :, rows].cpu()
     _compare(o_s, l_s, o_ref[:, rows], l_ref[:, :, rows], wl.name)
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
+@pytest.mark.gpu
+def test_fp8_paired_row_blocks_ragged_causal():
+    """Many units per CTA: row blocks are scheduled in pairs and aligned to the end of
+    the sequence; S = 16000 leaves a partial first block.  Sampled rows of two heads."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B, H, S = 2, 32, 16000
+    (q8, qs), (k8, ks), (v8, vs) = _case(16001, B, H, S, S)
+    scale = 1.0 / math.sqrt(128)
+    o, lse = pkg.attn_fwd_fp8(q8.to(DEV), k8.to(DEV), v8.to(DEV), q_scale=qs, k_scale=ks,
+                              v_scale=vs, causal=True, scale=scale)
+    assert pkg.attn_check() == pkg.ATTN_OK
+    heads = [3, 30]
+    rows = sorted({0, 1, 127, 128, 129, 255, 256, 383, 384, 7000, S - 257, S - 256, S - 129,
+                   S - 128, S - 2, S - 1})
+    sub = [t.view(torch.uint8)[:, :, heads].view(torch.float8_e4m3fn).to(torch.float64) * s
+           for t, s in ((q8, qs), (k8, ks), (v8, vs))]
+    o_ref, l_ref = attention_dense(*sub, scale, True, rows=rows)
+    o_s = o[:, rows][:, :, heads].cpu()
+    l_s = lse[:, heads][:, :, rows].cpu()
+    _compare(o_s, l_s, o_ref[:, rows], l_ref[:, :, rows], "fp8 paired blocks")

@@ -266,3 +266,39 @@ def test_cta_pair_kernel_varlen():
         compare(o, lse, o_ref, l_ref, what=f"pair varlen causal={causal}")
         a, b = int(cq[4]), int(cq[5])
         assert torch.all(o[a:b] == 0) and torch.all(torch.isneginf(lse[:, a:b]))
+
+
+def _boundary_rows(S, n_random, seed):
+    """Rows 0, S-1, both sides of every 128-row tile edge near the start and end of the
+    sequence (end-aligned causal blocks put the partial block first), plus seeded rows."""
+    edge = set()
+    for base in (0, S % 128, S % 256):
+        for t in range(4):
+            for d in (-1, 0, 1):
+                for r in (base + 128 * t + d, S - 1 - (base + 128 * t + d)):
+                    if 0 <= r < S:
+                        edge.add(r)
+    g = torch.Generator().manual_seed(seed)
+    edge.update((torch.randperm(S - 2, generator=g)[:n_random] + 1).tolist())
+    return sorted(edge | {0, S - 1})
+
+
+@pytest.mark.parametrize("D,dt", [(128, torch.bfloat16), (64, torch.float16)],
+                         ids=["cta_pair_d128", "single_cta_d64"])
+def test_paired_row_blocks_ragged_causal(D, dt):
+    """A causal problem with many units per worker: row blocks are scheduled in pairs
+    (heaviest with lightest of one head) and aligned to the end of the sequence, so
+    S = 16000 leaves a partial first block whose rows before 0 do not exist.  The oracle
+    checks rows at every tile edge near both ends and seeded rows of three heads."""
+    B, H, S = 2, 32, 16000
+    q, k, v = _dense_case(16000 + D, B, H, S, S, D, dt)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_gpu(q, k, v, True, scale)
+    heads = [0, 17, 31]
+    rows = _boundary_rows(S, 60, seed=D)
+    o_ref, l_ref = attention_dense(q[:, :, heads], k[:, :, heads], v[:, :, heads], scale, True,
+                                   rows=rows)
+    o_s = o[:, rows][:, :, heads].float().cpu().numpy()
+    l_s = lse[:, heads][:, :, rows].cpu().numpy()
+    compare(o_s, l_s, o_ref[:, rows], l_ref[:, :, rows], what=f"paired blocks D={D}")
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()

@@ -4,8 +4,8 @@ Such callers (a framework whose own allocator owns the GPU's memory, or a loop
 that cannot accept cudaMalloc's implicit synchronisation) get the same kernel
 with its scratch (the device error word) in a static device array.  This test
 calls it through the C ABI twice in a row and checks each output against the
-existing attn_fwd entry point within the parity tolerance.  The file name makes
-pytest collect it last.
+fp64 oracle and against the existing attn_fwd entry point, within the parity
+tolerance.  The file name makes pytest collect it last.
 """
 import ctypes
 import math
@@ -15,6 +15,7 @@ import pytest
 import torch
 
 import scaled_dot_product_tcgen05_gb300 as pkg
+from oracle.sdpa_oracle import attention_dense, attention_varlen
 from parity_helpers import compare
 
 pytestmark = pytest.mark.gpu
@@ -55,8 +56,14 @@ def test_noalloc_matches_attn_fwd_on_two_calls(case):
         shape = (int(cu[-1]), H, D)
         B, Sq, Sk = len(lens), int(cu[-1]), int(cu[-1])
         cu = cu.to(dev)
-    q, k, v = (torch.randn(shape, generator=g).to(dt).to(dev) for _ in range(3))
+    q_h, k_h, v_h = (torch.randn(shape, generator=g).to(dt) for _ in range(3))
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
     scale = 1.0 / math.sqrt(D)
+    if lens is None:
+        o_or, l_or = attention_dense(q_h, k_h, v_h, scale, causal)
+    else:
+        cu_h = cu.cpu()
+        o_or, l_or = attention_varlen(q_h, k_h, v_h, cu_h, cu_h, scale, causal)
     o_ref, lse_ref = pkg.attn_fwd(q, k, v, causal=causal, scale=scale, cu_seqlens_q=cu,
                                   cu_seqlens_k=cu)
     assert pkg.attn_check() == pkg.ATTN_OK
@@ -79,7 +86,9 @@ def test_noalloc_matches_attn_fwd_on_two_calls(case):
         if lens is not None:  # rows of the sequence without keys: O = 0, LSE = -inf in both
             sel_rows = torch.isneginf(lse_ref)
             assert torch.equal(torch.isneginf(lse), sel_rows)
-        compare(o, lse, np.where(sel, o_ref64, np.nan), l_ref64, what=f"noalloc call {call}")
+        compare(o, lse, o_or, l_or, what=f"noalloc call {call} vs the oracle")
+        compare(o, lse, np.where(sel, o_ref64, np.nan), l_ref64,
+                what=f"noalloc call {call} vs attn_fwd")
 
 
 def test_noalloc_rejects_bad_arguments_without_launching():
