@@ -5,6 +5,6 @@
 namespace attn {
 template cudaError_t launch_fwd<128, true>(const FwdParams&, int, cudaStream_t);
 namespace pair {
-template cudaError_t launch_fwd_2sm<true>(const FwdParams&, int, cudaStream_t);
+template cudaError_t launch_fwd_2sm<128, true>(const FwdParams&, int, cudaStream_t);
 }  // namespace pair
 }  // namespace attn

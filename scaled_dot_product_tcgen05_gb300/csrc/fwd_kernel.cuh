@@ -54,6 +54,7 @@ struct FwdParams {
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_kh;         // K with a 64-row box (pair kernel: each CTA loads half a tile)
+  CUtensorMap tm_vh;         // V halves of the pair kernel: box D/2 x 1 x 128, D-byte swizzle
   void* o;
   float* lse;
   const int32_t* cu_q;       // varlen only

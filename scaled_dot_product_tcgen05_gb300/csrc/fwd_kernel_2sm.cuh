@@ -1,18 +1,18 @@
-// Fused attention forward, head dim 128, on CTA pairs (clusters of 2) with
-// 2-SM tcgen05 MMAs and a triple-buffered score tile.
+// Fused attention forward on CTA pairs (clusters of 2) with 2-SM tcgen05 MMAs
+// and a triple-buffered score tile; head dim D = 64 or 128.
 //
 // Same computation as attn_fwd_kernel (see fwd_kernel.cuh for the definition
 // and its sources).  What changes is how the tensor cores are fed:
 //   * One M = 256 tcgen05.mma (cta_group::2), issued by the even CTA of the
 //     pair, covers 128 query rows of each CTA.  Each CTA reads only half of
-//     every K/V tile from shared memory (K: 64 of the 128 keys; V: 64 of the
-//     128 head-dim columns) and loads only that half with TMA.
+//     every K/V tile from shared memory (K: 64 of the 128 keys; V: D/2 of the
+//     D head-dim columns) and loads only that half with TMA.
 //   * Each CTA owns one 128-row query tile and three S buffers in tensor
 //     memory, so S(G+1) and S(G+2) = Q K^T are ready while the softmax works
 //     on S(G): the only ordering left is P(G) -> O += P(G) V(G) -> S(G+3)
 //     (P(G) is written over S(G), so S(G+3) reuses that buffer once P(G) has
 //     been consumed).  With two buffers the softmax waited for that chain.
-//   * TMEM per CTA: S buffers 0, 1, 2 | O (128 columns each, all 512 used).
+//   * TMEM per CTA: S buffers 0, 1, 2 (128 columns each) | O (D columns).
 //   * Two threads of the even CTA issue the MMAs: one the S = Q K^T products,
 //     one the O += P V products.  A single issuing thread was the bottleneck
 //     (each barrier poll and each 2-SM MMA issue costs it tens to hundreds of
@@ -34,9 +34,7 @@
 namespace attn {
 namespace pair {
 
-constexpr int D = 128;
 constexpr int kUR = 2 * kBM;    // query rows per pair unit
-constexpr int kStages = 5;      // K/V ring depth (half tiles: 16 KiB each)
 constexpr int kNBuf = 3;        // S buffers in tensor memory
 constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quarter: column halves 0 and 1
 constexpr int kEpiWarps = 4;    // one per TMEM lane quarter: O -> global memory
@@ -47,12 +45,17 @@ constexpr int kPLoad = 9;
 constexpr int kPPv = 10;        // issues O += P V
 constexpr int kPEpi = 11;       // first epilogue warp (11..14 cover the four lane quarters)
 
+template <int D>
 struct Layout {
-  static constexpr int kBlk = 16384;
-  static constexpr int kQTile = 2 * kBlk;          // 128 rows x 128 dims
-  static constexpr int kKHalf = 16384;             // 64 keys x 128 dims (two 8 KiB blocks)
-  static constexpr int kKBlk = 8192;
-  static constexpr int kVHalf = 16384;             // 128 keys x 64 dims (one block)
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kStages = D == 128 ? 5 : 8;  // K/V ring depth (half tiles)
+  static constexpr int kBlk = 16384;                // 128 rows x 128 B swizzle block
+  static constexpr int kQTile = (D / 64) * kBlk;    // 128 rows x D
+  static constexpr int kKBlk = 8192;                // 64 keys x 64 dims
+  static constexpr int kKHalf = (D / 64) * kKBlk;   // 64 keys x D
+  // 128 keys x D/2 dims: one 128-byte-swizzled block (D = 128) or rows of 64 B
+  // in 64-byte swizzle atoms (D = 64)
+  static constexpr int kVHalf = 128 * D;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kQTile;
   static constexpr int kVOff = kKOff + kStages * kKHalf;
@@ -68,13 +71,13 @@ struct Layout {
   static constexpr int kFillWords = 1 + 2 * kStages;
   // softmax exchange between the two warps of a row: per-step partial maxima
   // (two step parities x two halves x 128 rows) and the final row sums
-  static constexpr int kXMaxOff = kFillOff + 64;
+  static constexpr int kXMaxOff = kFillOff + (kFillWords * 4 + 15) / 16 * 16;
   static constexpr int kXSumOff = kXMaxOff + 2 * 2 * 128 * 4;
   // 1 / l of each row of the last finished unit, for the epilogue warps
   static constexpr int kInvLOff = kXSumOff + 2 * 128 * 2 * 4;
   static constexpr int kBytes = kInvLOff + 128 * 4;
   static constexpr int kAlloc = kBytes + 1024;
-  static constexpr uint32_t kColS = 0, kColO = kNBuf * 128;
+  static constexpr uint32_t kColS = 0, kColO = kNBuf * 128;  // O: D columns
   // Per-step barriers come in threes indexed by G % 3; barrier G % 3 completes
   // its phase G / 3 for step G.  No barrier can run two phases ahead of a
   // waiter:
@@ -152,7 +155,7 @@ __device__ __forceinline__ bool decode_pair(const FwdParams& p, int k, Cursor& c
 // c of this half with c < lo or c > limit are invisible (both already local to
 // the half).  Returns false if the wait before a rescale of O gave up (after
 // the step's named barrier).
-template <bool BF16>
+template <int D, bool BF16>
 __device__ __forceinline__ bool softmax_half_step(uint32_t tS, uint32_t tP, uint32_t tO, int lo,
                                                   int limit,
                                                   float cl, bool scale_pos, bool first,
@@ -233,7 +236,7 @@ __device__ __forceinline__ bool softmax_half_step(uint32_t tS, uint32_t tP, uint
     ptx::tc_fence_after();
     const uint64_t al2 = ptx::f2(alpha, alpha);
 #pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 32) {
+    for (int c0 = 0; c0 < D / 2; c0 += 32) {  // this half's D/2 columns of O
       uint32_t o[32];
       ptx::tmem_ld_x32(tO + c0, o);
 #pragma unroll
@@ -265,17 +268,17 @@ static __device__ __noinline__ void finish_row_barriers(const FwdParams& p, Curs
     for (int i = 0; n > 0 && i <= n; ++i) ptx::named_bar_sync(xbar, 64);
 }
 
-template <bool BF16>
+template <int D, bool BF16>
 __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, uint32_t bars,
                              uint8_t* base, const Ctl& ctl) {
-  using L = Layout;
+  using L = Layout<D>;
   const int warp = threadIdx.x >> 5;  // 0..7
   const int lane = threadIdx.x & 31;
   const int quarter = warp & 3;       // TMEM lane quarter (= SM sub-partition)
-  const int half = warp >> 2;         // columns [64 half, 64 half + 64) of S and O
+  const int half = warp >> 2;         // S columns [64 half, +64), O columns [D/2 half, +D/2)
   const int row = quarter * 32 + lane;
   const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
-  const uint32_t tO = tmem + lane_bits + L::kColO + half * 64;
+  const uint32_t tO = tmem + lane_bits + L::kColO + half * (D / 2);
   const uint32_t bar_p_lead = ptx::mapa(bars + 8 * L::PF, 0);  // + 8 * (G % 3)
   const uint32_t bar_lr = bars + 8 * L::LR, bar_lf = bars + 8 * L::LF;
   const uint32_t xbar = 1 + quarter;  // named barrier of the two warps of these rows
@@ -314,7 +317,7 @@ __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, u
         const uint32_t gp = G - 1;
         float* const xm = xmax + (G & 1u) * 256;
         const uint32_t tSb = tmem + lane_bits + L::kColS + b * 128;
-        if (!softmax_half_step<BF16>(tSb + 64 * half, tSb + 32 * half, tO, lo, limit, p.scale_log2,
+        if (!softmax_half_step<D, BF16>(tSb + 64 * half, tSb + 32 * half, tO, lo, limit, p.scale_log2,
                                      p.scale_pos != 0, j == 0, rs, xm + half * 128 + row,
                                      xm + (1 - half) * 128 + row, xbar,
                                      bars + 8 * (L::PVD + gp % kNBuf), (gp / kNBuf) & 1u, ctl)) {
@@ -355,10 +358,10 @@ __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, u
 // wait for 1 / l and for the unit's last O += P V, read O (all 128 columns)
 // out of tensor memory, release it to the next unit's products, then scale,
 // round and store the row.  The softmax warps meanwhile start the next unit.
-template <bool BF16>
+template <int D, bool BF16>
 __device__ void epilogue_role(const FwdParams& p, uint32_t rank, uint32_t tmem, uint32_t bars,
                               uint8_t* base, const Ctl& ctl) {
-  using L = Layout;
+  using L = Layout<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int quarter = warp & 3;  // TMEM lane quarter this warp may access
@@ -417,11 +420,11 @@ __device__ void epilogue_role(const FwdParams& p, uint32_t rank, uint32_t tmem, 
 
 // -------------------------------------------------------------------- MMA
 // S thread: lane 0 of warp kPMma of the even CTA.
-template <bool BF16>
+template <int D, bool BF16>
 __device__ void s_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint32_t bars,
                        const Ctl& ctl) {
-  using L = Layout;
-  constexpr int NS = kStages;
+  using L = Layout<D>;
+  constexpr int NS = L::kStages;
   constexpr uint32_t kIdS = ptx::idesc_f16_f32acc(BF16, 2 * kBM, kBN, false);
   constexpr uint16_t kBoth = 3;
   auto bar = [&](int i) { return bars + 8u * i; };
@@ -463,16 +466,20 @@ __device__ void s_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint32_
 }
 
 // PV thread: lane 0 of warp kPPv of the even CTA.
-template <bool BF16>
+template <int D, bool BF16>
 __device__ void pv_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint32_t bars,
                         const Ctl& ctl) {
-  using L = Layout;
-  constexpr int NS = kStages;
+  using L = Layout<D>;
+  constexpr int NS = L::kStages;
   constexpr uint32_t kIdPV = ptx::idesc_f16_f32acc(BF16, 2 * kBM, D, true);
   constexpr uint16_t kBoth = 3;
   auto bar = [&](int i) { return bars + 8u * i; };
   uint32_t g_base = 0;
-  const uint64_t dv0 = ptx::desc_sw128(smem + L::kVOff, L::kBlk, 1024);
+  // V half, MN-major (D/2 dims contiguous per key): one 128-byte swizzle atom
+  // column (D = 128) or one 64-byte one (D = 64); the next 8 keys follow at
+  // 8 rows x D bytes
+  const uint64_t dv0 = D == 128 ? ptx::desc_sw128(smem + L::kVOff, L::kBlk, 1024)
+                                : ptx::desc_sw64(smem + L::kVOff, L::kBlk, 512);
   const uint32_t tO = tmem + L::kColO;
   uint32_t u_cnt = 0;  // units with steps so far
   Cursor cur;
@@ -495,8 +502,8 @@ __device__ void pv_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint32
       const uint64_t dv = dv0 + ((st * L::kVHalf) >> 4);
       const uint32_t tP = tmem + L::kColS + (G % kNBuf) * 128;
 #pragma unroll
-      for (int ks = 0; ks < kBN / 16; ++ks)
-        ptx::mma_ts_pair(tO, tP + ks * 8, dv + ((ks * 2048) >> 4), kIdPV,
+      for (int ks = 0; ks < kBN / 16; ++ks)  // 16 keys = 2 atoms of 8 key rows x D bytes
+        ptx::mma_ts_pair(tO, tP + ks * 8, dv + ((ks * 16 * D) >> 4), kIdPV,
                          (j > 0 || ks > 0) ? 1u : 0u);
       ptx::mma_commit_pair(bar(L::VE + st), kBoth);
       ptx::mma_commit_pair(bar(L::PVD + G % kNBuf), kBoth);
@@ -509,26 +516,29 @@ __device__ void pv_loop(const FwdParams& p, uint32_t smem, uint32_t tmem, uint32
 
 // Each MMA thread makes sure its own tcgen05 operations retired before TMEM is
 // freed, also when its loop was abandoned.
+template <int D>
 __device__ __forceinline__ void mma_drain(uint32_t bars, const Ctl& ctl) {
-  const uint32_t done = bars + 8u * Layout::DONE;
+  const uint32_t done = bars + 8u * Layout<D>::DONE;
   ptx::mma_commit_pair(done, 1);
   wait_bar(done, 0, ctl, false);
 }
 
 // ------------------------------------------------------------------- load
+template <int NS>
 struct PairLoadLog {
   FillLog<1> q;
-  FillLog<kStages> k, v;
+  FillLog<NS> k, v;
 };
 
 // Runs on lane 0 of the load warp of both CTAs; each loads its own Q tile and
 // its half of every K/V tile, counting the bytes on the even CTA's barriers
 // (the even CTA arms each phase for both halves).  Every issued fill is
 // recorded in `f`.
+template <int D>
 static __device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bars, uint32_t rank,
-                                 const Ctl& ctl, PairLoadLog& f) {
-  using L = Layout;
-  constexpr int NS = kStages;
+                                 const Ctl& ctl, PairLoadLog<Layout<D>::kStages>& f) {
+  using L = Layout<D>;
+  constexpr int NS = L::kStages;
   const bool lead = rank == 0;
   auto bar = [&](int i) { return bars + 8u * i; };
   auto lbar = [&](int i) { return ptx::mapa(bars + 8u * i, 0); };
@@ -565,8 +575,8 @@ static __device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bar
       }
       if (it >= NS && !wait_bar(bar(L::VE + st), (it / NS - 1) & 1u, ctl)) return;
       if (lead) ptx::mbar_arrive_expect_tx(bar(L::VF + st), 2 * L::kVHalf);
-      ptx::tma_load_3d_pair(smem + L::kVOff + st * L::kVHalf, &p.tm_v, lbar(L::VF + st),
-                            64 * static_cast<int>(rank), w.h, krow);
+      ptx::tma_load_3d_pair(smem + L::kVOff + st * L::kVHalf, &p.tm_vh, lbar(L::VF + st),
+                            (D / 2) * static_cast<int>(rank), w.h, krow);
       f.v.last[st] = static_cast<int>(it);
     }
     kv_it += n;
@@ -580,6 +590,8 @@ static __device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bar
 // completed).  A fill the even CTA issued was armed for both halves; if the
 // odd CTA never sent its half, those bytes are counted here.  A fill only the
 // odd CTA issued was never armed; it is armed here for the odd half alone.
+// Such a repaired phase must not release a consumer: the caller repairs only
+// after the MMA threads have finished.
 __device__ __forceinline__ void settle_fill(uint32_t bar, int mine, int peer, int ring,
                                             uint32_t half_bytes, const Ctl& ctl) {
   const int last = max(mine, peer);
@@ -591,14 +603,16 @@ __device__ __forceinline__ void settle_fill(uint32_t bar, int mine, int peer, in
   wait_bar(bar, (static_cast<uint32_t>(last) / ring) & 1u, ctl, false);
 }
 
+template <int D>
 static __device__ void load_role(const FwdParams& p, uint32_t smem, uint8_t* base, uint32_t bars,
                                  uint32_t rank, const Ctl& ctl) {
-  using L = Layout;
-  PairLoadLog f;
+  using L = Layout<D>;
+  constexpr int kStages = L::kStages;
+  PairLoadLog<kStages> f;
   f.q.clear();
   f.k.clear();
   f.v.clear();
-  load_loop(p, smem, bars, rank, ctl, f);
+  load_loop<D>(p, smem, bars, rank, ctl, f);
   const uint32_t rec = smem + L::kFillOff;
   if (rank != 0) {
     // hand this CTA's record to the even CTA, whose barriers count our copies
@@ -615,7 +629,7 @@ static __device__ void load_role(const FwdParams& p, uint32_t smem, uint8_t* bas
   // Even CTA: no copy of the pair may land after either CTA exits (the odd one
   // leaves only after the closing cluster barrier, which this thread reaches
   // after the waits below).
-  PairLoadLog o = f;
+  PairLoadLog<kStages> o = f;
   if (wait_bar_cluster(bars + 8u * L::LDONE, 0, Ctl{ctl.abort_flag, ctl.err, ctl.timeout_ns},
                        false)) {
     const int* r = reinterpret_cast<const int*>(base + L::kFillOff);
@@ -626,6 +640,14 @@ static __device__ void load_role(const FwdParams& p, uint32_t smem, uint8_t* bas
       o.v.last[st] = r[1 + kStages + st];
     }
   }
+  // The records differ only if a loader stopped early or a fill was skipped:
+  // then the MMA threads may still be waiting for the phases about to be
+  // repaired, so wait (bounded) until both have finished (they always do,
+  // every one of their waits being bounded) before repairing any.
+  bool differ = f.q.last[0] != o.q.last[0];
+  for (int st = 0; st < kStages; ++st)
+    differ = differ || f.k.last[st] != o.k.last[st] || f.v.last[st] != o.v.last[st];
+  if (differ) wait_bar(bars + 8u * L::DONE, 0, ctl, false);
   settle_fill(bars + 8u * L::QF, f.q.last[0], o.q.last[0], 1, L::kQTile, ctl);
 #pragma unroll 1
   for (int st = 0; st < kStages; ++st) {
@@ -635,10 +657,10 @@ static __device__ void load_role(const FwdParams& p, uint32_t smem, uint8_t* bas
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool BF16>
+template <int D, bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     attn_fwd_kernel_2sm(const __grid_constant__ FwdParams p) {
-  using L = Layout;
+  using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t smem = (raw + 1023u) & ~1023u;
@@ -670,7 +692,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   if (warp == kPLoad && lane == 0) {
     ptx::tma_prefetch_desc(&p.tm_q);
     ptx::tma_prefetch_desc(&p.tm_kh);
-    ptx::tma_prefetch_desc(&p.tm_v);
+    ptx::tma_prefetch_desc(&p.tm_vh);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -679,21 +701,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   const Ctl ctl{abort_flag, p.err, p.timeout_ns};
 
   if (warp < kSoftmaxWarps) {
-    softmax_role<BF16>(p, rank, tmem, bars, base, ctl);
+    softmax_role<D, BF16>(p, rank, tmem, bars, base, ctl);
   } else if (warp == kPMma) {
     if (lane == 0 && rank == 0) {
-      s_loop<BF16>(p, smem, tmem, bars, ctl);
-      mma_drain(bars, ctl);
+      s_loop<D, BF16>(p, smem, tmem, bars, ctl);
+      mma_drain<D>(bars, ctl);
     }
   } else if (warp == kPPv) {
     if (lane == 0 && rank == 0) {
-      pv_loop<BF16>(p, smem, tmem, bars, ctl);
-      mma_drain(bars, ctl);
+      pv_loop<D, BF16>(p, smem, tmem, bars, ctl);
+      mma_drain<D>(bars, ctl);
     }
   } else if (warp == kPLoad) {
-    if (lane == 0) load_role(p, smem, base, bars, rank, ctl);
+    if (lane == 0) load_role<D>(p, smem, base, bars, rank, ctl);
   } else {
-    epilogue_role<BF16>(p, rank, tmem, bars, base, ctl);
+    epilogue_role<D, BF16>(p, rank, tmem, bars, base, ctl);
   }
 
   ptx::tc_fence_before();
@@ -703,20 +725,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   if (warp == kPMma) ptx::tmem_dealloc_pair(tmem, kTmemCols);
 }
 
+template <int D>
 inline int fwd_2sm_smem_bytes(const FwdParams& p) {
-  return Layout::kAlloc + (seq_ordered(p) ? kOrderBytes : 0);
+  return Layout<D>::kAlloc + (seq_ordered(p) ? kOrderBytes : 0);
 }
 
-template <bool BF16>
+template <int D, bool BF16>
 cudaError_t launch_fwd_2sm(const FwdParams& params, int grid, cudaStream_t stream) {
   FwdParams p = params;
-  p.order_off = Layout::kBytes;  // the packed-sequence order follows the layout
-  const void* fn = reinterpret_cast<const void*>(&attn_fwd_kernel_2sm<BF16>);
+  p.order_off = Layout<D>::kBytes;  // the packed-sequence order follows the layout
+  const void* fn = reinterpret_cast<const void*>(&attn_fwd_kernel_2sm<D, BF16>);
   static std::atomic<unsigned long long> opted{0};
-  const cudaError_t e = smem_opt_in(fn, Layout::kAlloc + kOrderBytes, opted);
+  const cudaError_t e = smem_opt_in(fn, Layout<D>::kAlloc + kOrderBytes, opted);
   if (e != cudaSuccess) return e;
   void* args[] = {&p};
-  return cudaLaunchKernel(fn, dim3(grid), dim3(kPairThreads), args, fwd_2sm_smem_bytes(p),
+  return cudaLaunchKernel(fn, dim3(grid), dim3(kPairThreads), args, fwd_2sm_smem_bytes<D>(p),
                           stream);
 }
 

@@ -137,21 +137,22 @@ inline bool on_device(const void* p, int dev) {
   return ok;
 }
 
-// [rows, H, D] 16-bit tensor, box = box_rows rows x 1 head x 64 elements
-// (128 B), 128-byte swizzle, zero fill outside the tensor.
+// [rows, H, D] 16-bit tensor, box = box_rows rows x 1 head x box_cols elements
+// (128 B by default, with 128-byte swizzle; 32 elements = 64 B with 64-byte
+// swizzle), zero fill outside the tensor.
 inline int encode_rows_heads_dim(CUtensorMap* m, const void* ptr, long long rows, int H, int D,
-                                 bool bf16, int box_rows = kBM) {
+                                 bool bf16, int box_rows = kBM, int box_cols = 64) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                            static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(D) * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), 1, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = encoder_slot()(
       m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
       const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -232,7 +233,8 @@ inline int prepare_fwd(const void* q, const void* k, const void* v, void* o, flo
   if (encode_rows_heads_dim(&p->tm_q, q, call.rows_q, H, D, call.bf16) != ATTN_OK ||
       encode_rows_heads_dim(&p->tm_k, k, call.rows_k, H, D, call.bf16) != ATTN_OK ||
       encode_rows_heads_dim(&p->tm_v, v, call.rows_k, H, D, call.bf16) != ATTN_OK ||
-      encode_rows_heads_dim(&p->tm_kh, k, call.rows_k, H, D, call.bf16, kBN / 2) != ATTN_OK)
+      encode_rows_heads_dim(&p->tm_kh, k, call.rows_k, H, D, call.bf16, kBN / 2) != ATTN_OK ||
+      encode_rows_heads_dim(&p->tm_vh, v, call.rows_k, H, D, call.bf16, kBN, D / 2) != ATTN_OK)
     return ATTN_ERR_CUDA;
   p->o = o;
   p->lse = lse;

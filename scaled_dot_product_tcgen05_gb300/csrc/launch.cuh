@@ -13,8 +13,10 @@ extern template cudaError_t launch_fwd<64, true>(const FwdParams&, int, cudaStre
 extern template cudaError_t launch_fwd<128, false>(const FwdParams&, int, cudaStream_t);
 extern template cudaError_t launch_fwd<128, true>(const FwdParams&, int, cudaStream_t);
 namespace pair {
-extern template cudaError_t launch_fwd_2sm<false>(const FwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_fwd_2sm<true>(const FwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_fwd_2sm<64, false>(const FwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_fwd_2sm<64, true>(const FwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_fwd_2sm<128, false>(const FwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_fwd_2sm<128, true>(const FwdParams&, int, cudaStream_t);
 }  // namespace pair
 
 // Fills the visibility fields of `p` (see FwdParams) from the C arguments:
@@ -54,25 +56,33 @@ inline int pair_blocks_for(long long units, long long workers) {
   return units >= 16 * workers ? 1 : 0;
 }
 
-// Head dim 128 runs on CTA pairs with 2-SM MMAs; head dim 64 on single CTAs.
-// ATTN_PAIR=0 sends head dim 128 to the single-CTA kernel as well (kept for
-// cross-checks).  The grid is persistent: at most one CTA per SM.
+// Kernel choice.  Head dim 128 runs on CTA pairs with 2-SM MMAs.  Head dim 64
+// runs on CTA pairs without a causal mask and on single CTAs with one (measured
+// on GB300: pairs 689 vs 648 TFLOP/s at B=8 H=12 S=2048 non-causal, single
+// CTAs 521 vs 470 causal, within 2-3 % of each other on long sequences).
+// ATTN_PAIR=0 forces single CTAs, ATTN_PAIR=1 CTA pairs (cross-checks).  The
+// grid is persistent: at most one CTA per SM.
 inline cudaError_t launch_forward(const FwdParams& params, int D, bool bf16, bool varlen, int B,
                                   int H, long long rows_q, int Sq, int sms, cudaStream_t s,
                                   LaunchInfo* info) {
   FwdParams p = params;
   const char* sel = std::getenv("ATTN_PAIR");
-  const bool use_pair = D == 128 && sms >= 2 && !(sel != nullptr && sel[0] == '0');
+  const bool forced = sel != nullptr && (sel[0] == '0' || sel[0] == '1');
+  const bool use_pair =
+      sms >= 2 && (forced ? sel[0] == '1' : (D == 128 || p.causal == 0));
   if (use_pair) {
     const long long units = units_bound(varlen, B, H, rows_q, Sq, pair::kUR);
     const long long pairs = units < sms / 2 ? units : sms / 2;
     p.pair_blocks = pair_blocks_for(units, pairs);
     info->grid = static_cast<int>(2 * pairs);
-    info->smem = pair::fwd_2sm_smem_bytes(p);
+    info->smem = D == 64 ? pair::fwd_2sm_smem_bytes<64>(p) : pair::fwd_2sm_smem_bytes<128>(p);
     info->pair = true;
     if (pairs <= 0) return cudaSuccess;
-    return bf16 ? pair::launch_fwd_2sm<true>(p, info->grid, s)
-                : pair::launch_fwd_2sm<false>(p, info->grid, s);
+    if (D == 64)
+      return bf16 ? pair::launch_fwd_2sm<64, true>(p, info->grid, s)
+                  : pair::launch_fwd_2sm<64, false>(p, info->grid, s);
+    return bf16 ? pair::launch_fwd_2sm<128, true>(p, info->grid, s)
+                : pair::launch_fwd_2sm<128, false>(p, info->grid, s);
   }
   const long long units = units_bound(varlen, B, H, rows_q, Sq, kUnitRows);
   info->grid = static_cast<int>(units < sms ? units : sms);

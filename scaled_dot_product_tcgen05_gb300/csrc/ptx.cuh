@@ -141,6 +141,19 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo_byte
   return d;
 }
 
+// The same for a 64-byte-swizzled operand (atoms of 8 rows x 64 B on 512-byte
+// boundaries; swizzle mode 4).
+__device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr, uint32_t lbo_bytes,
+                                              uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(4) << 61;
+  return d;
+}
+
 // Instruction descriptor for kind::f16 with an fp32 accumulator.
 //   bits 4-5 D type (1 = f32)   bits 7-9 A type, 10-12 B type (0 = f16, 1 = bf16)
 //   bit 15 A major (0 = K)      bit 16 B major (1 = MN)

@@ -4,8 +4,8 @@ Every device-side wait is bounded (ATTN_WAIT_TIMEOUT_MS); when one runs out the
 kernel writes the error word, its roles drain and the CTA exits, so the
 context stays usable and attn_check reports ATTN_ERR_DEVICE_TIMEOUT.  The
 injected faults (ATTN_INJECT_FAULT) are a tile fill that is never issued (1:
-block 0 of the forward kernels -- the CTA-pair kernel for head dim 128 and the
-single-CTA kernel for head dim 64 -- skips its first K tile, block 0 of the
+block 0 of the forward kernels -- the CTA-pair kernel, and the single-CTA
+kernel that ATTN_PAIR=0 selects -- skips its first K tile, block 0 of the
 decode kernel its first fill, so a wait runs out) and an empty launch grid that
 the launch itself rejects (2, decode only: ATTN_ERR_CUDA).  Neither traps,
 faults or hangs the GPU.  The forward cases run units with more K/V tiles than
@@ -143,14 +143,16 @@ def test_debug_log_names_each_launch(capfd):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("D", [128, 64], ids=["cta_pair_kernel", "single_cta_kernel"])
-def test_forward_bounded_wait_runs_out_and_the_context_stays_usable(D):
+@pytest.mark.parametrize("D,pair", [(128, "1"), (64, "1"), (64, "0")],
+                         ids=["cta_pair_d128", "cta_pair_d64", "single_cta_d64"])
+def test_forward_bounded_wait_runs_out_and_the_context_stays_usable(D, pair, monkeypatch):
     """attn_fwd with a K tile that never arrives: every role of the affected CTAs winds
     down within the time limit, the call reports ATTN_ERR_DEVICE_TIMEOUT, and the same
     call without the fault then matches the oracle on the same context.  S = 1000 gives
     the first unit of pair / block 0 eight K/V tiles, more than either ring holds."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+    monkeypatch.setenv("ATTN_PAIR", pair)
     g = torch.Generator().manual_seed(47 + D)
     B, S, H = 1, 1000, 4
     q, k, v = (torch.randn(B, S, H, D, generator=g).to(torch.bfloat16) for _ in range(3))
