@@ -2,12 +2,15 @@
 
 One step = one fused forward (O and LSE) over the long-context causal workload
 B=1, H=32, Sq=Sk=65536, D=128, bf16 (inputs 1.5 GiB, larger than the 129 MB
-L2, so no flush is needed between steps).  Throughput is TFLOP/s with the
+L2, so no flush is needed between steps; workloads whose step touches less
+than twice the L2 are timed step by step with the L2 flushed in between).
+Throughput is TFLOP/s with the
 FLOP count 4*B*H*Sq*Sk*D, halved for causal; for a sliding-window workload
 (--workload window128k_causal) 4*D per visible (query, key) pair, counted
 exactly.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--seed S]
+                  [--heads H]   (the workload with H heads: a reduced case for profiling)
   python bench.py --impl reference ...   (the fp64 CPU oracle on a bounded sample)
 
 Under torchrun the job is N times the workload, sharded by whole batches: rank r
@@ -39,6 +42,7 @@ DEFAULT_WORKLOAD = "long64k_causal"
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 FALLBACK_PEAK_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 10 ** 6  # GB300 L2
 
 
 # ----------------------------------------------------------------------------- ranks
@@ -190,12 +194,14 @@ def source_digest(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def kernel_name(D: int, decode: bool = False) -> str:
-    """The kernel attn_fwd launches (head dim 128 runs on CTA pairs unless ATTN_PAIR=0)."""
+def kernel_name(D: int, decode: bool = False, causal: bool = True) -> str:
+    """The kernel attn_fwd launches: CTA pairs for head dim 128 and for head dim 64
+    without a causal mask, single CTAs otherwise (ATTN_PAIR=0 / 1 forces one)."""
     if decode:
         return "attn_decode_kernel"
-    return "attn_fwd_kernel_2sm" if D == 128 and os.environ.get("ATTN_PAIR") != "0" \
-        else "attn_fwd_kernel"
+    sel = os.environ.get("ATTN_PAIR")
+    pair = sel == "1" if sel in ("0", "1") else (D == 128 or not causal)
+    return "attn_fwd_kernel_2sm" if pair else "attn_fwd_kernel"
 
 
 def profiled_traffic(workload: str, kernel: str):
@@ -448,6 +454,9 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=192)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="run the workload with this many heads (0: its own); reduced "
+                         "cases for profiling, not the benchmark")
     ap.add_argument("--seed", type=int, default=0,
                     help="another seeded draw of the same workload (0: the standard draw)")
     args = ap.parse_args(argv)
@@ -455,9 +464,15 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
 
     wl = reseed_workload(W.standard_workloads()[args.workload], args.seed)
+    if args.heads:
+        if not 1 <= args.heads <= wl.H:
+            raise SystemExit(f"--heads must be in 1..{wl.H}")
+        wl = dataclasses.replace(wl, H=args.heads)
     flops, nbytes, cfg = workload_info(wl)
     if args.seed:
         cfg = dict(cfg, seed=args.seed)
+    if args.heads:
+        cfg = dict(cfg, reduced_heads=args.heads)
     ws, rank, local = dist_env()
 
     if args.impl == "reference":
@@ -547,6 +562,13 @@ def main(argv=None):
         launches_per_step = 2  # V transpose, attention
     if wl.decode and pkg.decode_workspace_bytes(wl.B, wl.H, wl.Sq, wl.Sk, wl.D) > 0:
         launches_per_step = 2  # the split decode kernel and the merge kernel
+    # Inputs that could stay in L2 from one step to the next are evicted between
+    # timed steps by writing a buffer twice the L2's size; each step is then timed
+    # alone (its own pair of events) and the flush stays outside the timed steps.
+    step_bytes = sum(t.numel() * t.element_size() for t in bs0.values())
+    flush = None
+    if step_bytes < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     sampler = ClockSampler(local)
     sampler.start()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -554,6 +576,9 @@ def main(argv=None):
     barrier()
     torch.cuda.synchronize()
     for i in range(args.steps):
+        if flush is not None:
+            with torch.cuda.stream(stream):
+                flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -564,9 +589,17 @@ def main(argv=None):
     if st != pkg.ATTN_OK:
         raise SystemExit(f"device status {pkg.status_string(st)}")
     launch_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = ev[0][0].elapsed_time(ev[-1][1])
+    if flush is None:  # back to back: the whole region
+        total_ms = ev[0][0].elapsed_time(ev[-1][1])
+    else:  # the steps alone, without the flushes between them
+        total_ms = sum(launch_ms)
     ms_step = max_over_ranks(total_ms / args.steps, dev)
     kernel_ms = sum(launch_ms) / len(launch_ms)
+    l2_note = ("no flush: a step touches %.2f GiB > twice the %d MB L2" %
+               (step_bytes / 2 ** 30, L2_BYTES // 10 ** 6) if flush is None else
+               "L2 flushed between timed steps (%d MB written; a step touches %.1f MB)" %
+               (2 * L2_BYTES // 10 ** 6, step_bytes / 1e6))
+    del flush
 
     # ---- end to end through the public API, host buffers, copies inside the region
     o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
@@ -649,7 +682,7 @@ def main(argv=None):
     else:
         peak, peak_src = peaks()
         achieved = flops / (kernel_ms * 1e-3) / 1e12
-        kern = kernel_name(wl.D)
+        kern = kernel_name(wl.D, causal=wl.causal)
         per_step = flops * ws / 1e12
         unit, metric, bound = "TFLOP/s", "attention fwd TFLOP/s", "tensor"
         if wl.backward:
@@ -660,13 +693,13 @@ def main(argv=None):
             achieved = flops / (kernel_ms * 1e-3) / 1e12
             kern = "attn_fwd_fp8_kernel"
             metric = "attention fwd fp8 TFLOP/s"
-    traffic = profiled_traffic(wl.name, kern)
+    traffic = None if args.heads else profiled_traffic(wl.name, kern)  # a full launch's bytes
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_sample(wl, args.cpu_budget_s)
     cfg = dict(cfg, parallelism=f"dp{ws}: rank r processes shard r (own inputs)" if ws > 1
                else "single GPU",
-               l2="no flush: inputs %.2f GiB > 129 MB L2" % (h2d / 2 ** 30),
+               l2=l2_note,
                grid_ctas=grid, smem_bytes=smem)
     out = {
         "metric": metric, "value": per_step / (ms_step * 1e-3),

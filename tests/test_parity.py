@@ -203,36 +203,38 @@ def test_host_and_misplaced_pointers_rejected():
     assert st == pkg.ATTN_ERR_INVALID_ARG
 
 
-def test_grid_is_persistent():
-    q, k, v = _dense_case(6, 1, 32, 4096, 4096, 128, torch.bfloat16)
-    run_gpu(q, k, v, True, 0.088)
-    grid, smem = pkg.last_launch()
-    assert grid == 2 * (pkg.num_sms() // 2) and smem <= 232448
-    q, k, v = _dense_case(7, 1, 32, 4096, 4096, 64, torch.bfloat16)
-    run_gpu(q, k, v, True, 0.125)
+def test_grid_is_persistent(monkeypatch):
+    # CTA pairs (head dim 128; head dim 64 without a causal mask): one pair per two SMs
+    for D, seed, causal in ((128, 6, True), (64, 7, False)):
+        q, k, v = _dense_case(seed, 1, 32, 4096, 4096, D, torch.bfloat16)
+        run_gpu(q, k, v, causal, 1 / math.sqrt(D))
+        grid, smem = pkg.last_launch()
+        assert grid == 2 * (pkg.num_sms() // 2) and smem <= 232448
+    run_gpu(q, k, v, True, 0.125)  # head dim 64, causal: single CTAs, one per SM
     grid, smem = pkg.last_launch()
     assert grid == pkg.num_sms() and smem <= 232448
 
 
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("case", [
     (2, 3, 700, 700, torch.bfloat16, True),
     (1, 2, 300, 520, torch.float16, False),
 ], ids=["dense_bf16_causal", "dense_fp16_q300_k520"])
-def test_single_cta_kernel_head_dim_128(case, monkeypatch):
-    """Head dim 128 runs on CTA pairs; ATTN_PAIR=0 keeps the single-CTA kernel covered."""
+def test_single_cta_kernel(case, D, monkeypatch):
+    """Both head dims run on CTA pairs; ATTN_PAIR=0 keeps the single-CTA kernel covered."""
     monkeypatch.setenv("ATTN_PAIR", "0")
     B, H, Sq, Sk, dt, causal = case
-    q, k, v = _dense_case(Sq + 3 * Sk, B, H, Sq, Sk, 128, dt)
-    o, lse = run_gpu(q, k, v, causal, 1 / math.sqrt(128))
+    q, k, v = _dense_case(Sq + 3 * Sk + D, B, H, Sq, Sk, D, dt)
+    o, lse = run_gpu(q, k, v, causal, 1 / math.sqrt(D))
     grid, _ = pkg.last_launch()
     assert grid <= pkg.num_sms()
-    o_ref, l_ref = attention_dense(q, k, v, 1 / math.sqrt(128), causal)
-    compare(o, lse, o_ref, l_ref, what=f"1sm {case}")
+    o_ref, l_ref = attention_dense(q, k, v, 1 / math.sqrt(D), causal)
+    compare(o, lse, o_ref, l_ref, what=f"1sm D={D} {case}")
     lens = [300, 1, 129, 0, 900]
-    qv, kv, vv, cq, ck = _varlen(13, lens, lens, 2, 128, torch.bfloat16)
+    qv, kv, vv, cq, ck = _varlen(13, lens, lens, 2, D, torch.bfloat16)
     o, lse = run_gpu(qv, kv, vv, True, 0.1, cq, ck)
     o_ref, l_ref = attention_varlen(qv, kv, vv, cq, ck, 0.1, True)
-    compare(o, lse, o_ref, l_ref, what="1sm varlen")
+    compare(o, lse, o_ref, l_ref, what=f"1sm D={D} varlen")
 
 
 PAIR_CASES = [
@@ -243,24 +245,28 @@ PAIR_CASES = [
 ]
 
 
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: "B{}H{}q{}k{}{}{}".format(
     c[0], c[1], c[2], c[3], "bf" if c[4] == torch.bfloat16 else "fp", "c" if c[5] else ""))
-def test_cta_pair_kernel(case):
-    """Head dim 128 on CTA pairs (2-SM MMAs)."""
+def test_cta_pair_kernel(case, D, monkeypatch):
+    """Both head dims on CTA pairs (2-SM MMAs)."""
+    monkeypatch.setenv("ATTN_PAIR", "1")
     B, H, Sq, Sk, dt, causal = case
-    q, k, v = _dense_case(Sq + 5 * Sk, B, H, Sq, Sk, 128, dt)
-    o, lse = run_gpu(q, k, v, causal, 1 / math.sqrt(128))
+    q, k, v = _dense_case(Sq + 5 * Sk + D, B, H, Sq, Sk, D, dt)
+    o, lse = run_gpu(q, k, v, causal, 1 / math.sqrt(D))
     grid, _ = pkg.last_launch()
     assert grid % 2 == 0
-    o_ref, l_ref = attention_dense(q, k, v, 1 / math.sqrt(128), causal)
-    compare(o, lse, o_ref, l_ref, what=f"pair {case}")
+    o_ref, l_ref = attention_dense(q, k, v, 1 / math.sqrt(D), causal)
+    compare(o, lse, o_ref, l_ref, what=f"pair D={D} {case}")
 
 
-def test_cta_pair_kernel_varlen():
+@pytest.mark.parametrize("D", [128, 64])
+def test_cta_pair_kernel_varlen(D, monkeypatch):
+    monkeypatch.setenv("ATTN_PAIR", "1")
     for causal in (False, True):
         lens_q = [1, 0, 300, 129, 5, 256, 1000]
         lens_k = [1, 7, 300, 129, 0, 100, 1000]
-        q, k, v, cq, ck = _varlen(14, lens_q, lens_k, 3, 128, torch.bfloat16)
+        q, k, v, cq, ck = _varlen(14, lens_q, lens_k, 3, D, torch.bfloat16)
         o, lse = run_gpu(q, k, v, causal, 0.09, cq, ck)
         o_ref, l_ref = attention_varlen(q, k, v, cq, ck, 0.09, causal)
         compare(o, lse, o_ref, l_ref, what=f"pair varlen causal={causal}")
@@ -302,3 +308,77 @@ def test_paired_row_blocks_ragged_causal(D, dt):
     l_s = lse[:, heads][:, :, rows].cpu().numpy()
     compare(o_s, l_s, o_ref[:, rows], l_ref[:, :, rows], what=f"paired blocks D={D}")
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
+# Unit roundoff of the 16-bit P and O: 2^-8 (bf16, 8 significant bits), 2^-11 (fp16).
+_U16 = {torch.bfloat16: 2.0 ** -8, torch.float16: 2.0 ** -11}
+
+
+def _equal_scores_case(pattern, S, D, dt):
+    """Q = e_0 in every row, K[j, 0] in {0, 1} by ``pattern``, V constant per head.
+
+    Every score is 0 or scale, so a row's probabilities take two values, each shared by
+    hundreds of keys.  ``scale`` is chosen so that the smaller (A, C2) or the larger
+    (C1) of the two exponentials lies 0.45 of a unit in the last place above a 16-bit
+    value: its rounding to 16 bits, made once per key, is as large as it gets short of
+    a tie, and every one of those keys carries it.
+      A  : key j scores high iff j % 64 == 0 (a high key in every half tile, so the
+           row max is known from the first tile on and the low keys are below it);
+      C1 : the first half of the keys low, the second half high by a factor 2^4 in
+           probability (within the kernels' 2^8 rescale threshold, so a row that meets
+           the low keys first keeps its stale max and the high keys' values exceed 1);
+      C2 : the first half high, the second half low.
+    """
+    u_bits = 8 if dt == torch.bfloat16 else 11  # significant bits
+    q = torch.zeros(1, S, 2, D)
+    q[..., 0] = 1.0
+    k = torch.zeros(1, S, 2, D)
+    j = torch.arange(S)
+    if pattern == "A":
+        k[0, j % 64 == 0, :, 0] = 1.0
+        small = 0.5 * (1.0 + 0.45 * 2.0 ** (1 - u_bits))  # in [1/2, 1): ulp = 2^-u_bits
+        scale = -math.log(small)
+    else:
+        high = (j >= S // 2) if pattern == "C1" else (j < S // 2)
+        k[0, high, :, 0] = 1.0
+        big = 16.0 * (1.0 + 0.45 * 2.0 ** (1 - u_bits))  # in [16, 32): ulp = 16·2^(1-u_bits)
+        scale = math.log(big)
+    v = torch.empty(1, S, 2, D)
+    v[:, :, 0] = 100.0  # exact in both 16-bit formats
+    v[:, :, 1] = -37.25
+    return q.to(dt), k.to(dt), v.to(dt), scale
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("D", [128, 64])
+@pytest.mark.parametrize("pattern", ["A", "C1", "C2"])
+def test_many_equal_rounded_probabilities(pattern, D, dt, causal):
+    """The one-sum denominator with constant V of large magnitude.
+
+    The kernels normalise O by the exact row sum plus, once per tile and thread, the
+    16-bit rounding error of the thread's largest probability, while P.V uses every
+    rounded probability.  When hundreds of keys share one probability value whose
+    rounding is close to half a unit, the numerator carries that rounding hundreds of
+    times and the denominator once per tile.  With V = c in every row the exact O is c,
+    and the kernel's O is c·(Σ p̃)/(Σ p + corrections): its relative error is at most
+    the unit roundoff u of the rounded probabilities, plus u for the 16-bit output,
+    plus fp32 summation error (≤ 1e-4 at these lengths).  So |O - c| ≤ (2u + 1e-4)·|c|.
+    That bound scales with |V|; the parity tolerance of 2e-2 is for V of unit size.
+    The LSE uses the exact sum and meets the usual relative bound.
+    """
+    S = 1000  # several 128-key tiles and 256-row units, ragged tail
+    q, k, v, scale = _equal_scores_case(pattern, S, D, dt)
+    o, lse = run_gpu(q, k, v, causal, scale)
+    o_ref, l_ref = attention_dense(q, k, v, scale, causal)
+    u = _U16[dt]
+    c = v.double()[0, 0, :, 0].numpy()  # per head
+    bound = (2 * u + 1e-4) * np.abs(c)
+    og = o.double().cpu().numpy()
+    err = np.abs(og - o_ref)  # [1, S, H, D]
+    worst = err.max(axis=(0, 1, 3))
+    assert np.all(worst <= bound), f"{pattern} D={D} {dt}: |O - c| {worst} > bound {bound}"
+    assert np.allclose(o_ref, c[None, None, :, None], rtol=1e-12, atol=0)
+    lg = lse.double().cpu().numpy()
+    rel = np.abs(lg - l_ref) / np.maximum(1.0, np.abs(l_ref))
+    assert rel.max() <= 1e-3, f"LSE {rel.max()}"
