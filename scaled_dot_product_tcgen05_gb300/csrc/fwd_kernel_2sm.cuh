@@ -63,7 +63,8 @@ struct Layout {
   static constexpr int QF = 0, QE = 1, KF = 2, KE = KF + kStages, VF = KE + kStages,
                        VE = VF + kStages, SF = VE + kStages, PF = SF + kNBuf,
                        PVD = PF + kNBuf, OF = PVD + kNBuf, DONE = OF + 1, LDONE = DONE + 1,
-                       LR = LDONE + 1, LF = LR + 1, OFREE = LF + 1, kNumBars = OFREE + 1;
+                       LR = LDONE + 1, LF = LR + 1, OFREE = LF + 1, DR = OFREE + 1,
+                       kNumBars = DR + 2;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   // the odd CTA's loader record (last Q fill, last K / V fill per stage),
   // written into the even CTA before it arrives on LDONE
@@ -75,7 +76,11 @@ struct Layout {
   static constexpr int kXSumOff = kXMaxOff + 2 * 2 * 128 * 4;
   // 1 / l of each row of the last finished unit, for the epilogue warps
   static constexpr int kInvLOff = kXSumOff + 2 * 128 * 2 * 4;
-  static constexpr int kBytes = kInvLOff + 128 * 4;
+  // Two unit descriptors for the softmax warps (unit k in slot k % 2), written
+  // one unit ahead by the epilogue warps: a header and each row's visible keys.
+  static constexpr int kDescOff = kInvLOff + 128 * 4;
+  static constexpr int kDescBytes = 32 + 2 * 128 * 4;
+  static constexpr int kBytes = kDescOff + 2 * kDescBytes;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t kColS = 0, kColO = kNBuf * 128;  // O: D columns
   // Per-step barriers come in threes indexed by G % 3; barrier G % 3 completes
@@ -98,6 +103,13 @@ struct Layout {
   static constexpr uint32_t kLrArrivals = kSoftmaxWarps / 2;
   static constexpr uint32_t kLfArrivals = kEpiWarps;
   static constexpr uint32_t kOFreeArrivals = 2 * kEpiWarps;
+  // Descriptor k is complete (DR + k % 2, phase k / 2 % 2) when every epilogue
+  // warp has written its rows.  The slot of unit k is written again for unit
+  // k + 2 only in the epilogue's iteration k + 1, which follows its wait for
+  // LR of unit k; the softmax warps read descriptor k at the start of unit k,
+  // before they publish LR of unit k.  So no slot or phase is overwritten
+  // before it is read.
+  static constexpr uint32_t kDrArrivals = kEpiWarps;
 };
 
 // Same as wait_bar, but with cluster-scope acquire (used where the peer CTA arrives).
@@ -254,18 +266,71 @@ __device__ __forceinline__ bool softmax_half_step(uint32_t tS, uint32_t tP, uint
   return true;
 }
 
+// What the softmax warps need of unit k, published by the epilogue warps one
+// unit ahead (they decode every unit anyway), so that the softmax warps spend
+// nothing on decoding between units.  Followed in the slot by int lo[128],
+// hi[128]: the visible keys (inclusive, within the sequence) of each row of
+// this CTA's tile (row_keys), for units with n > 0.
+struct UnitDesc {
+  int valid;       // 0: the walk has ended (no unit k)
+  int n;           // K/V steps of the pair
+  int j0;          // first K/V tile
+  int q0;          // first query row of this CTA's tile (may be < 0)
+  int Lq;          // query rows of the sequence
+  int pad;
+  long long lse0;  // LSE index of row 0 of the sequence and head (row q adds q)
+};
+static_assert(sizeof(UnitDesc) == 32, "descriptor header");
+
+// Epilogue warp of lane quarter `quarter`: writes its 32 rows of descriptor k
+// (and, for quarter 0, the header), then arrives on DR + k % 2.
+template <int D>
+__device__ __forceinline__ void publish_desc(const FwdParams& p, uint32_t rank, uint8_t* base,
+                                             uint32_t bars, int k, bool valid, const Unit& w,
+                                             int n, int quarter, int lane) {
+  using L = Layout<D>;
+  uint8_t* const slot = base + L::kDescOff + (k & 1) * L::kDescBytes;
+  int* const lo = reinterpret_cast<int*>(slot + sizeof(UnitDesc));
+  const int row = quarter * 32 + lane;
+  const int q0 = valid ? q0_of(w, static_cast<int>(rank)) : 0;
+  if (valid && n > 0) {
+    int key_lo, key_hi;
+    row_keys(p, w, q0 + row, key_lo, key_hi);
+    lo[row] = key_lo;
+    lo[128 + row] = key_hi;
+  }
+  if (quarter == 0 && lane == 0) {
+    UnitDesc d;
+    d.valid = valid ? 1 : 0;
+    d.n = valid ? n : 0;
+    d.j0 = valid ? w.j0 : 0;
+    d.q0 = q0;
+    d.Lq = valid ? w.Lq : 0;
+    d.pad = 0;
+    d.lse0 = !valid ? 0
+             : p.varlen ? static_cast<long long>(w.h) * p.Sq + w.q_start
+                        : (static_cast<long long>(w.b) * p.H + w.h) * p.Sq;
+    *reinterpret_cast<UnitDesc*>(slot) = d;
+  }
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(bars + 8u * (L::DR + (k & 1)));
+}
+
 // After a wait of a softmax warp gave up: the warp's remaining arrivals at its
-// named barrier -- `pending` of the current unit k, then n + 1 for every later
-// unit with n steps (one per step and the closing exchange of the row sums).
-// The two warps of a row walk the same units and steps, so the partner warp,
-// which may have passed the same wait, never stays at that barrier.
-static __device__ __noinline__ void finish_row_barriers(const FwdParams& p, Cursor cur, int k,
+// named barrier -- `pending` of the current unit, then n + 1 for every unit
+// from k_first on with n > 0 steps (one per step and the closing exchange of
+// the row sums).  The two warps of a row walk the same units and steps (the
+// units of the descriptors, which come from the same decode), so the partner
+// warp, which may have passed the same wait, never stays at that barrier.
+static __device__ __noinline__ void finish_row_barriers(const FwdParams& p, int k_first,
                                                         int pending, uint32_t xbar) {
   for (int i = 0; i < pending; ++i) ptx::named_bar_sync(xbar, 64);
+  Cursor cur;
+  init_cursor<kUR>(p, cur, false);
   Unit w;
   int n = 0;
-  for (++k; decode_pair(p, k, cur, w, n, false); ++k)
-    for (int i = 0; n > 0 && i <= n; ++i) ptx::named_bar_sync(xbar, 64);
+  for (int k = 0; decode_pair(p, k, cur, w, n, false); ++k)
+    for (int i = 0; k >= k_first && n > 0 && i <= n; ++i) ptx::named_bar_sync(xbar, 64);
 }
 
 template <int D, bool BF16>
@@ -287,27 +352,30 @@ __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, u
   float* const inv_l_slot = reinterpret_cast<float*>(base + L::kInvLOff);
   uint32_t lr_cnt = 0, g_base = 0;
 
-  Cursor cur;
-  init_cursor<kUR>(p, cur, false);
-  Unit w;
-  int n = 0;
-  for (int k = 0; decode_pair(p, k, cur, w, n, false); ++k) {
-    const int qrow = q0_of(w, static_cast<int>(rank)) + row;
-    const bool row_ok = qrow >= 0 && qrow < w.Lq;
-    const long long lidx = p.varlen
-                               ? static_cast<long long>(w.h) * p.Sq + w.q_start + qrow
-                               : (static_cast<long long>(w.b) * p.H + w.h) * p.Sq + qrow;
+  for (int k = 0;; ++k) {
+    if (!wait_bar_warp(bars + 8u * (L::DR + (k & 1)), (static_cast<uint32_t>(k) >> 1) & 1u,
+                       ctl)) {
+      finish_row_barriers(p, k, 0, xbar);
+      return;
+    }
+    const uint8_t* const slot = base + L::kDescOff + (k & 1) * L::kDescBytes;
+    const UnitDesc d = *reinterpret_cast<const UnitDesc*>(slot);
+    if (!d.valid) break;
+    const int n = d.n;
+    const int qrow = d.q0 + row;
+    const bool row_ok = qrow >= 0 && qrow < d.Lq;
+    const long long lidx = d.lse0 + qrow;
     RowState rs{-INFINITY, 0.0f, 0.0f};
     if (n > 0) {
-      int key_lo, key_hi;  // visible keys of this row, shifted to this half's columns
-      row_keys(p, w, qrow, key_lo, key_hi);
-      key_lo -= 64 * half;
-      key_hi -= 64 * half;
-      for (int j = 0, kb = w.j0 * kBN; j < n; ++j, kb += kBN) {
+      // visible keys of this row, shifted to this half's columns
+      const int* const keys = reinterpret_cast<const int*>(slot + sizeof(UnitDesc));
+      const int key_lo = keys[row] - 64 * half;
+      const int key_hi = keys[128 + row] - 64 * half;
+      for (int j = 0, kb = d.j0 * kBN; j < n; ++j, kb += kBN) {
         const uint32_t G = g_base + j;
         const uint32_t b = G % kNBuf;
         if (!wait_bar_warp(bars + 8 * (L::SF + b), (G / kNBuf) & 1u, ctl)) {
-          finish_row_barriers(p, cur, k, n - j + 1, xbar);
+          finish_row_barriers(p, k + 1, n - j + 1, xbar);
           return;
         }
         ptx::tc_fence_after();
@@ -321,7 +389,7 @@ __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, u
                                      p.scale_pos != 0, j == 0, rs, xm + half * 128 + row,
                                      xm + (1 - half) * 128 + row, xbar,
                                      bars + 8 * (L::PVD + gp % kNBuf), (gp / kNBuf) & 1u, ctl)) {
-          finish_row_barriers(p, cur, k, n - j, xbar);
+          finish_row_barriers(p, k + 1, n - j, xbar);
           return;
         }
         ptx::tc_fence_before();
@@ -335,16 +403,19 @@ __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, u
       ptx::named_bar_sync(xbar, 64);
       rs.l_p += xsum[((1 - half) * 128 + row) * 2 + 0];
       rs.l_x += xsum[((1 - half) * 128 + row) * 2 + 1];
-      if (half == 0) {  // hand 1 / l to the epilogue warps once they have read the last one
-        if (lr_cnt > 0 && !wait_bar_warp(bar_lf, (lr_cnt - 1) & 1u, ctl)) {
-          finish_row_barriers(p, cur, k, 0, xbar);
-          return;
-        }
-        inv_l_slot[row] = rs.l_p > 0.0f ? 1.0f / rs.l_p : 0.0f;
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_lr);
-        ++lr_cnt;
+    }
+    // Hand 1 / l to the epilogue warps once they have read the last one.  Every
+    // unit does this, even one without steps: the epilogue waits for it before
+    // writing the unit's rows, which keeps it at most one descriptor ahead.
+    if (half == 0) {
+      if (lr_cnt > 0 && !wait_bar_warp(bar_lf, (lr_cnt - 1) & 1u, ctl)) {
+        finish_row_barriers(p, k + 1, 0, xbar);
+        return;
       }
+      inv_l_slot[row] = rs.l_p > 0.0f ? 1.0f / rs.l_p : 0.0f;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar_lr);
+      ++lr_cnt;
     }
     // rows without any visible key (n = 0) get LSE = -inf; their O = 0 is
     // written by the epilogue warps
@@ -355,9 +426,10 @@ __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, u
 }
 
 // Epilogue warps (one per TMEM lane quarter, thread = query row): per unit,
-// wait for 1 / l and for the unit's last O += P V, read O (all 128 columns)
-// out of tensor memory, release it to the next unit's products, then scale,
-// round and store the row.  The softmax warps meanwhile start the next unit.
+// publish the descriptor of the next unit for the softmax warps, wait for
+// 1 / l and for the unit's last O += P V, read O (all D columns) out of
+// tensor memory, release it to the next unit's products, then scale, round
+// and store the row.  The softmax warps meanwhile start the next unit.
 template <int D, bool BF16>
 __device__ void epilogue_role(const FwdParams& p, uint32_t rank, uint32_t tmem, uint32_t bars,
                               uint8_t* base, const Ctl& ctl) {
@@ -371,16 +443,27 @@ __device__ void epilogue_role(const FwdParams& p, uint32_t rank, uint32_t tmem, 
   const uint32_t bar_free_lead = ptx::mapa(bars + 8 * L::OFREE, 0);
   const float* const inv_l_slot = reinterpret_cast<const float*>(base + L::kInvLOff);
   uint16_t* const O = static_cast<uint16_t*>(p.o);
-  uint32_t cnt = 0;
+  uint32_t lr_cnt = 0, of_cnt = 0;
 
   Cursor cur;
   init_cursor<kUR>(p, cur, false);
-  Unit w;
-  int n = 0;
-  for (int k = 0; decode_pair(p, k, cur, w, n, false); ++k) {
+  Unit w_next;
+  int n_next = 0;
+  bool more = decode_pair(p, 0, cur, w_next, n_next, false);
+  publish_desc<D>(p, rank, base, bars, 0, more, w_next, n_next, quarter, lane);
+  for (int k = 0; more; ++k) {
+    const Unit w = w_next;
+    const int n = n_next;
+    more = decode_pair(p, k + 1, cur, w_next, n_next, false);
+    publish_desc<D>(p, rank, base, bars, k + 1, more, w_next, n_next, quarter, lane);
     const int qrow = q0_of(w, static_cast<int>(rank)) + row;
     const bool row_ok = qrow >= 0 && qrow < w.Lq;
     const long long orow = (static_cast<long long>(w.q_start) + qrow) * p.H + w.h;
+    if (!wait_bar_warp(bar_lr, lr_cnt & 1u, ctl)) return;
+    ++lr_cnt;
+    const float inv_l = inv_l_slot[row];
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar_lf);
     if (n == 0) {  // no visible key: O = 0
       if (row_ok) {
         uint4* const dst = reinterpret_cast<uint4*>(O + orow * D);
@@ -389,12 +472,8 @@ __device__ void epilogue_role(const FwdParams& p, uint32_t rank, uint32_t tmem, 
       }
       continue;
     }
-    if (!wait_bar_warp(bar_lr, cnt & 1u, ctl)) return;
-    const float inv_l = inv_l_slot[row];
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(bar_lf);
-    if (!wait_bar_warp(bar_of, cnt & 1u, ctl)) return;
-    ++cnt;
+    if (!wait_bar_warp(bar_of, of_cnt & 1u, ctl)) return;
+    ++of_cnt;
     ptx::tc_fence_after();
     uint4* const dst = reinterpret_cast<uint4*>(O + (row_ok ? orow : 0) * D);
 #pragma unroll
@@ -679,6 +758,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                                     : i == L::LR                    ? L::kLrArrivals
                                     : i == L::LF                    ? L::kLfArrivals
                                     : i == L::OFREE                 ? L::kOFreeArrivals
+                                    : i >= L::DR                    ? L::kDrArrivals
                                                                     : 1u);
     *abort_flag = 0;
     ptx::fence_mbar_init();
