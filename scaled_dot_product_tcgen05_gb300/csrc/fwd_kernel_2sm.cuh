@@ -418,8 +418,9 @@ __device__ void softmax_role(const FwdParams& p, uint32_t rank, uint32_t tmem, u
       ++lr_cnt;
     }
     // rows without any visible key (n = 0) get LSE = -inf; their O = 0 is
-    // written by the epilogue warps
-    if (row_ok && half == 0) {
+    // written by the epilogue warps.  Both halves hold the same sums and max
+    // after the exchange; half 1 writes the LSE while half 0 hands over 1 / l.
+    if (row_ok && half == 1) {
       p.lse[lidx] = rs.l_x > 0.0f ? (rs.m + ptx::lg2(rs.l_x)) * 0.69314718055994531f : -INFINITY;
     }
   }
