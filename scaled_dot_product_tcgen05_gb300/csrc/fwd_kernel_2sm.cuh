@@ -444,6 +444,8 @@ __device__ void epilogue_role(const FwdParams& p, uint32_t rank, uint32_t tmem, 
   const uint32_t bar_free_lead = ptx::mapa(bars + 8 * L::OFREE, 0);
   const float* const inv_l_slot = reinterpret_cast<const float*>(base + L::kInvLOff);
   uint16_t* const O = static_cast<uint16_t*>(p.o);
+  // rows are D * 2 bytes apart: 32-byte stores whenever O itself is 32-byte aligned
+  const bool o32 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
   uint32_t lr_cnt = 0, of_cnt = 0;
 
   Cursor cur;
@@ -486,10 +488,19 @@ __device__ void epilogue_role(const FwdParams& p, uint32_t rank, uint32_t tmem, 
       for (int i = 0; i < 32; ++i)
         pk[i] = ptx::pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
                                  __uint_as_float(o[2 * i + 1]) * inv_l);
-      if (row_ok)
+      if (row_ok) {
+        if (o32) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          dst[c0 / 8 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int i = 0; i < 4; ++i)
+            ptx::st_global_v8(dst + c0 / 8 + 2 * i, pk[8 * i], pk[8 * i + 1], pk[8 * i + 2],
+                              pk[8 * i + 3], pk[8 * i + 4], pk[8 * i + 5], pk[8 * i + 6],
+                              pk[8 * i + 7]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[c0 / 8 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
     }
     // every load of O has completed (tcgen05.ld waits): the next unit may overwrite it
     ptx::tc_fence_before();

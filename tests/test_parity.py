@@ -145,9 +145,14 @@ def test_varlen_edges(causal, D, dt):
     assert torch.all(o[a:b] == 0) and torch.all(torch.isneginf(lse[:, a:b]))
 
 
-def test_poisoned_outputs_and_guard_bands():
-    """Writes land only on valid rows: guards and rows outside every sequence keep NaN."""
-    H, D, dt = 2, 128, torch.bfloat16
+@pytest.mark.parametrize("D,causal,guard", [(128, True, 4096), (128, True, 4104),
+                                             (64, False, 4104), (64, True, 4104)],
+                         ids=["pair_o32", "pair_o16", "pair_d64_o16", "single_d64_o16"])
+def test_poisoned_outputs_and_guard_bands(D, causal, guard):
+    """Writes land only on valid rows: guards and rows outside every sequence keep NaN.
+    A guard of 4104 elements puts O 16 bytes off a 32-byte boundary, so the rows are
+    written with 16-byte stores instead of 32-byte ones."""
+    H, dt = 2, torch.bfloat16
     lens = [130, 3, 250]
     q, k, v, cq, ck = _varlen(12, lens, lens, H, D, dt)
     Tq = int(cq[-1])
@@ -155,18 +160,17 @@ def test_poisoned_outputs_and_guard_bands():
     dev = torch.device("cuda:0")
     qd = torch.cat([q, torch.randn(pad_rows, H, D).to(dt)]).to(dev)
     kd, vd = k.to(dev), v.to(dev)
-    guard = 4096
     o_buf = torch.full(((Tq + pad_rows) * H * D + 2 * guard,), float("nan"), dtype=dt, device=dev)
     l_buf = torch.full((H * (Tq + pad_rows) + 2 * guard,), float("nan"), device=dev)
     o = o_buf[guard:guard + (Tq + pad_rows) * H * D].view(Tq + pad_rows, H, D)
     lse = l_buf[guard:guard + H * (Tq + pad_rows)].view(H, Tq + pad_rows)
-    pkg.attn_fwd(qd, kd, vd, causal=True, cu_seqlens_q=cq.to(dev), cu_seqlens_k=ck.to(dev),
+    pkg.attn_fwd(qd, kd, vd, causal=causal, cu_seqlens_q=cq.to(dev), cu_seqlens_k=ck.to(dev),
                  out=o, lse=lse)
     assert pkg.attn_check() == pkg.ATTN_OK
     assert torch.isnan(o_buf[:guard]).all() and torch.isnan(o_buf[-guard:]).all()
     assert torch.isnan(l_buf[:guard]).all() and torch.isnan(l_buf[-guard:]).all()
     assert torch.isnan(o[Tq:]).all() and torch.isnan(lse[:, Tq:]).all()
-    o_ref, l_ref = attention_varlen(q, k, v, cq, ck, 1 / math.sqrt(D), True)
+    o_ref, l_ref = attention_varlen(q, k, v, cq, ck, 1 / math.sqrt(D), causal)
     compare(o[:Tq], lse[:, :Tq], o_ref, l_ref, what="poisoned")
 
 
