@@ -73,6 +73,10 @@ struct FwdParams {
   // Schedule items pair the row blocks i and nU-1-i of one (sequence, head)
   // (see decode_rows); set by the host when the units far outnumber the workers.
   int pair_blocks = 0;
+  // Dense calls only: units ordered row block first, (batch, head) second
+  // (see decode_rows); set by the host when every head's K and V fit in L2
+  // together, so that no head needs its CTAs to run side by side.
+  int block_major = 0;
   // Offset (from the 1024-aligned origin of the dynamic shared memory) of the
   // packed-sequence walk order, past every other buffer of the kernel; set by
   // the host, which adds kOrderBytes to the launch when the order is used.
@@ -278,7 +282,10 @@ __device__ __forceinline__ void set_block(const FwdParams& p, Unit& w, int nU, i
 // its sequence, head and block of UR query rows.
 // Order: (sequence, head) outer, row blocks inner.  Keeping one head's blocks
 // together keeps the K/V tiles that the concurrently running workers stream
-// within L2 (one head of a 64K-token sequence is 32 MB).  Without
+// within L2 (one head of a 64K-token sequence is 32 MB).  A dense call whose
+// K and V fit in L2 as a whole (p.block_major) orders row blocks outer and
+// (batch, head) inner instead: the blocks then come heaviest first across all
+// heads, so the snake deal ends level even with few units per worker.  Without
 // p.pair_blocks, u enumerates the blocks of a (sequence, head), heaviest
 // causal block first.  With p.pair_blocks, u = 2 s + part: schedule item s
 // holds block nU-1-i (part 0, the heaviest under a causal mask) and block i
@@ -294,9 +301,16 @@ __device__ __forceinline__ bool decode_rows(const FwdParams& p, int u, Cursor& c
   if (!VL || !p.varlen) {
     nU = (p.Sq + UR - 1) / UR;
     const int per = p.pair_blocks ? (nU + 1) / 2 : nU;
-    if (s >= p.B * p.H * per) return false;
-    const int bh = s / per;
-    i = s - bh * per;
+    const int heads = p.B * p.H;
+    if (s >= heads * per) return false;
+    int bh;
+    if (p.block_major) {
+      i = s / heads;
+      bh = s - i * heads;
+    } else {
+      bh = s / per;
+      i = s - bh * per;
+    }
     w.b = bh / p.H;
     w.h = bh - w.b * p.H;
     w.q_start = w.b * p.Sq;
