@@ -43,6 +43,7 @@ constexpr int kUnitRows = kBM * kTiles;  // query rows per work unit
 constexpr int kThreads = 320;            // 8 softmax warps + MMA warp + load warp
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
+constexpr int kTileSoftmaxWarps = 8;     // warps 0-3: query tile 0, warps 4-7: query tile 1
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;     // rescale O only if max grows by > 2^8
 constexpr int kUnbounded = 1 << 30;      // window side without a bound
@@ -86,6 +87,8 @@ struct FwdParams {
   int inject = 0;
 };
 
+constexpr int kDescSlots = 4;     // unit descriptors in flight (single-CTA kernel)
+
 template <int D>
 struct Layout {
   static_assert(D == 64 || D == 128, "head dim");
@@ -99,9 +102,13 @@ struct Layout {
   // barrier indices
   static constexpr int QF = 0, QE = 1, KF = 2, KE = KF + kStages, VF = KE + kStages,
                        VE = VF + kStages, SF = VE + kStages, PF = SF + 2, OF = PF + 2,
-                       DONE = OF + 2, kNumBars = DONE + 1;
+                       DONE = OF + 2, DRY = DONE + 1, DFR = DRY + kDescSlots,
+                       kNumBars = DFR + kDescSlots;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag
-  static constexpr int kBytes = kMiscOff + 16;
+  // Ring of unit descriptors the loader publishes for the softmax warps (unit
+  // k in slot k % kDescSlots: "ready" DRY + slot, "free" DFR + slot).
+  static constexpr int kDescOff = kMiscOff + 16;
+  static constexpr int kBytes = kDescOff + kDescSlots * 48;
   static constexpr int kAlloc = kBytes + 1024;             // slack for 1024-B alignment
   // TMEM columns
   static constexpr uint32_t kColS = 0, kColO = 256;
@@ -556,9 +563,54 @@ __device__ __forceinline__ bool softmax_step_pv(uint32_t tS, uint32_t tO, int lo
   return true;
 }
 
+// What the softmax warps need of unit k, published by the loader thread (which
+// decodes every unit first anyway), so that the softmax warps spend nothing on
+// decoding between units.
+struct TileUnitDesc {
+  int more;        // 0: the walk has ended (no unit k)
+  int n0, n1;      // K/V steps of query tile 0 / 1
+  int valid;       // bit t: query tile t holds rows of the sequence
+  int q0;          // first query row of tile 0 (may be < 0)
+  int Lq, Lk;      // rows and keys of the sequence
+  int j0;          // first K/V tile
+  long long o0;    // O row index (rows of [rows, H]) of sequence row 0, this head
+  long long lse0;  // LSE index of sequence row 0, this head
+};
+static_assert(sizeof(TileUnitDesc) == 48, "descriptor");
+
+// Loader: writes descriptor k (more = false: the end of the walk) once the
+// softmax warps have read descriptor k - kDescSlots from the same slot.
+template <int D>
+__device__ __forceinline__ bool publish_tile_desc(const FwdParams& p, uint8_t* base,
+                                                  uint32_t bars, int k, bool more, const Unit& w,
+                                                  const Ctl& ctl) {
+  using L = Layout<D>;
+  const int slot = k % kDescSlots;
+  if (k >= kDescSlots &&
+      !wait_bar(bars + 8u * (L::DFR + slot), (static_cast<uint32_t>(k / kDescSlots) - 1u) & 1u,
+                ctl))
+    return false;
+  TileUnitDesc d;
+  d.more = more ? 1 : 0;
+  d.n0 = more ? w.n[0] : 0;
+  d.n1 = more ? w.n[1] : 0;
+  d.valid = more ? (w.valid[0] ? 1 : 0) | (w.valid[1] ? 2 : 0) : 0;
+  d.q0 = more ? w.q0 : 0;
+  d.Lq = more ? w.Lq : 0;
+  d.Lk = more ? w.Lk : 0;
+  d.j0 = more ? w.j0 : 0;
+  d.o0 = more ? static_cast<long long>(w.q_start) * p.H + w.h : 0;
+  d.lse0 = !more ? 0
+           : p.varlen ? static_cast<long long>(w.h) * p.Sq + w.q_start
+                      : (static_cast<long long>(w.b) * p.H + w.h) * p.Sq;
+  *reinterpret_cast<TileUnitDesc*>(base + L::kDescOff + slot * 48) = d;
+  ptx::mbar_arrive(bars + 8u * (L::DRY + slot));
+  return true;
+}
+
 template <int D, bool BF16>
 __device__ void softmax_role(const FwdParams& p, int t, uint32_t tmem, uint32_t bars,
-                             const Ctl& ctl) {
+                             const uint8_t* base, const Ctl& ctl) {
   using L = Layout<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -574,24 +626,29 @@ __device__ void softmax_role(const FwdParams& p, int t, uint32_t tmem, uint32_t 
   using out_t = uint16_t;
   out_t* const O = static_cast<out_t*>(p.o);
 
-  Cursor cur;
-  init_cursor<kUnitRows>(p, cur, false);
-  Unit w;
-  for (int k = 0; decode_unit(p, slot_unit(p, k), cur, w, false); ++k) {
-    if (!(t == 0 ? w.valid[0] : w.valid[1])) continue;
-    const int q0 = w.q0 + t * kBM;
+  for (int k = 0;; ++k) {
+    const int slot = k % kDescSlots;
+    if (!wait_bar_warp(bars + 8u * (L::DRY + slot), static_cast<uint32_t>(k / kDescSlots) & 1u,
+                       ctl))
+      return;
+    const TileUnitDesc d = *reinterpret_cast<const TileUnitDesc*>(base + L::kDescOff + slot * 48);
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bars + 8u * (L::DFR + slot));
+    if (!d.more) break;
+    if (((d.valid >> t) & 1) == 0) continue;
+    const int q0 = d.q0 + t * kBM;
     const int qrow = q0 + row;
-    const bool row_ok = qrow >= 0 && qrow < w.Lq;
-    const int n = t == 0 ? w.n[0] : w.n[1];
-    const long long orow = (static_cast<long long>(w.q_start) + qrow) * p.H + w.h;
-    const long long lidx = p.varlen
-                               ? static_cast<long long>(w.h) * p.Sq + w.q_start + qrow
-                               : (static_cast<long long>(w.b) * p.H + w.h) * p.Sq + qrow;
+    const bool row_ok = qrow >= 0 && qrow < d.Lq;
+    const int n = t == 0 ? d.n0 : d.n1;
+    const long long orow = d.o0 + static_cast<long long>(qrow) * p.H;
+    const long long lidx = d.lse0 + qrow;
     RowState rs{-INFINITY, 0.0f, 0.0f};
     if (n > 0) {
       int key_lo, key_hi;
-      row_keys(p, w, qrow, key_lo, key_hi);
-      for (int j = 0, kb = w.j0 * kBN; j < n; ++j, kb += kBN) {
+      Unit wk;  // row_keys reads the key count only
+      wk.Lk = d.Lk;
+      row_keys(p, wk, qrow, key_lo, key_hi);
+      for (int j = 0, kb = d.j0 * kBN; j < n; ++j, kb += kBN) {
         if (!wait_bar_warp(bar_s, s_cnt & 1u, ctl)) return;
         ++s_cnt;
         ptx::tc_fence_after();
@@ -735,8 +792,8 @@ struct LoadLog {
 };
 
 template <int D>
-__device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bars, const Ctl& ctl,
-                          LoadLog<D>& f) {
+__device__ void load_loop(const FwdParams& p, uint32_t smem, uint8_t* base, uint32_t bars,
+                          const Ctl& ctl, LoadLog<D>& f) {
   using L = Layout<D>;
   constexpr int NS = L::kStages;
   auto bar = [&](int i) { return bars + 8u * i; };
@@ -744,7 +801,9 @@ __device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bars, cons
   Cursor cur;
   init_cursor<kUnitRows>(p, cur, true);
   Unit w;
-  for (int k = 0; decode_unit(p, slot_unit(p, k), cur, w, true); ++k) {
+  int k = 0;
+  for (; decode_unit(p, slot_unit(p, k), cur, w, true); ++k) {
+    if (!publish_tile_desc<D>(p, base, bars, k, true, w, ctl)) return;
     const int nmax = max(w.n[0], w.n[1]);
     if (nmax == 0) continue;
     if (q_it > 0 && !wait_bar(bar(L::QE), (q_it - 1) & 1u, ctl)) return;
@@ -782,16 +841,18 @@ __device__ void load_loop(const FwdParams& p, uint32_t smem, uint32_t bars, cons
     }
     kv_it += nmax;
   }
+  publish_tile_desc<D>(p, base, bars, k, false, w, ctl);
 }
 
 template <int D>
-__device__ void load_role(const FwdParams& p, uint32_t smem, uint32_t bars, const Ctl& ctl) {
+__device__ void load_role(const FwdParams& p, uint32_t smem, uint8_t* base, uint32_t bars,
+                          const Ctl& ctl) {
   using L = Layout<D>;
   LoadLog<D> f;
   f.q.clear();
   f.k.clear();
   f.v.clear();
-  load_loop<D>(p, smem, bars, ctl, f);
+  load_loop<D>(p, smem, base, bars, ctl, f);
   // No TMA write may land after the CTA exits: wait for the last copy issued
   // into each buffer (normally these phases completed long ago).
   drain_fills(bars, L::QF, f.q, ctl);
@@ -815,7 +876,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i)
-      ptx::mbar_init(bars + 8u * i, (i == L::PF || i == L::PF + 1) ? kBM : 1u);
+      ptx::mbar_init(bars + 8u * i, (i == L::PF || i == L::PF + 1) ? kBM
+                                    : (i >= L::DFR)                  ? kTileSoftmaxWarps
+                                                                     : 1u);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -836,11 +899,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const Ctl ctl{abort_flag, p.err, p.timeout_ns};
 
   if (warp < kMmaWarp) {
-    softmax_role<D, BF16>(p, warp >> 2, tmem, bars, ctl);
+    softmax_role<D, BF16>(p, warp >> 2, tmem, bars, base, ctl);
   } else if (warp == kMmaWarp) {
     if (lane == 0) mma_role<D, BF16>(p, smem, tmem, bars, ctl);
   } else if (lane == 0) {
-    load_role<D>(p, smem, bars, ctl);
+    load_role<D>(p, smem, base, bars, ctl);
   }
 
   ptx::tc_fence_before();
