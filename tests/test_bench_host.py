@@ -160,3 +160,19 @@ def test_seed_selects_another_draw_of_the_same_workload():
                 assert x.base_seed // 1000 == w.wid
     with pytest.raises(SystemExit):
         bench.reseed_workload(wl, 10)
+
+
+def test_l2_flush_only_for_steps_that_fit_in_l2():
+    """Workloads whose step touches less than twice the L2 are flushed between timed
+    steps (the 2K, 512 and tiny ones); the long, packed, window, decode and backward
+    workloads are not."""
+    l2 = bench.L2_BYTES
+    assert bench.l2_flush_bytes(2 * l2) == 0
+    assert bench.l2_flush_bytes(2 * l2 - 1) == 2 * l2
+    assert bench.l2_flush_bytes(0) == 2 * l2
+XX, True), ("mha512_causal", True), ("tiny_causal", True),
+                          ("long64k_causal", False), ("varlen_causal", False),
+                          ("window128k_causal", False), ("decode128k_q1", False)]:
+        w = wl[name]
+        _, nbytes, _ = bench.workload_info(w)  # inputs read and outputs written once
+        assert (bench.l2_flush_bytes(int(nbytes)) > 0) == flushed, name
