@@ -170,7 +170,8 @@ def test_l2_flush_only_for_steps_that_fit_in_l2():
     assert bench.l2_flush_bytes(2 * l2) == 0
     assert bench.l2_flush_bytes(2 * l2 - 1) == 2 * l2
     assert bench.l2_flush_bytes(0) == 2 * l2
-XX, True), ("mha512_causal", True), ("tiny_causal", True),
+    wl = bench.W.standard_workloads()
+    for name, flushed in [("mha2k_bf16_causal", True), ("mha512_causal", True), ("tiny_causal", True),
                           ("long64k_causal", False), ("varlen_causal", False),
                           ("window128k_causal", False), ("decode128k_q1", False)]:
         w = wl[name]
