@@ -177,3 +177,24 @@ def test_l2_flush_only_for_steps_that_fit_in_l2():
         w = wl[name]
         _, nbytes, _ = bench.workload_info(w)  # inputs read and outputs written once
         assert (bench.l2_flush_bytes(int(nbytes)) > 0) == flushed, name
+
+
+def test_committed_profiles_match_the_kernel_sources():
+    """Every ncu summary under profiles/ names a benchmarked kernel and workload and
+    records the digest of that kernel's sources; bench.py reports its DRAM traffic only
+    while the digest matches, so a summary left behind by a kernel change shows here."""
+    import re
+    names = os.listdir(bench.PROFILE_DIR)
+    assert names, "no profiles committed"
+    wls = bench.W.standard_workloads()
+    for name in names:
+        assert name.endswith(".md"), name
+        kernel = next((k for k in sorted(bench.KERNEL_SOURCES, key=len, reverse=True)
+                       if name.startswith(k + "_")), None)
+        assert kernel is not None, name
+        workload = name[len(kernel) + 1:-3]
+        assert workload in wls, name
+        text = open(os.path.join(bench.PROFILE_DIR, name)).read()
+        m = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+        assert m and m.group(1) == bench.source_digest(kernel), f"{name}: stale digest"
+        assert bench.profiled_traffic(workload, kernel) > 0, name
