@@ -178,9 +178,9 @@ __device__ void dec_compute(const DecParams& p, uint8_t* base, uint32_t bars, co
         const uint8_t* kt = base + L::kKOff + st * L::kTile;
         const uint8_t* vt = base + L::kVOff + st * L::kTile;
         // ---- s_t = q_t . k_r (scaled, log2 units), one key per lane
-        float s0[SQ], s1[SQ];
+        uint64_t acc[SQ];  // (even dims, odd dims) partial sums of q_t . k_r
 #pragma unroll
-        for (int t = 0; t < SQ; ++t) s0[t] = s1[t] = 0.0f;
+        for (int t = 0; t < SQ; ++t) acc[t] = 0ull;
 #pragma unroll
         for (int cc = 0; cc < D / 8; ++cc) {
           const int blk = cc >> 3, c = cc & 7;
@@ -195,14 +195,10 @@ __device__ void dec_compute(const DecParams& p, uint8_t* base, uint32_t bars, co
           for (int t = 0; t < SQ; ++t) {
             const float4 qa = *reinterpret_cast<const float4*>(qs + t * D + cc * 8);
             const float4 qb = *reinterpret_cast<const float4*>(qs + t * D + cc * 8 + 4);
-            s0[t] = fmaf(kf[0], qa.x, s0[t]);
-            s1[t] = fmaf(kf[1], qa.y, s1[t]);
-            s0[t] = fmaf(kf[2], qa.z, s0[t]);
-            s1[t] = fmaf(kf[3], qa.w, s1[t]);
-            s0[t] = fmaf(kf[4], qb.x, s0[t]);
-            s1[t] = fmaf(kf[5], qb.y, s1[t]);
-            s0[t] = fmaf(kf[6], qb.z, s0[t]);
-            s1[t] = fmaf(kf[7], qb.w, s1[t]);
+            acc[t] = ptx::f2_fma(ptx::f2(kf[0], kf[1]), ptx::f2(qa.x, qa.y), acc[t]);
+            acc[t] = ptx::f2_fma(ptx::f2(kf[2], kf[3]), ptx::f2(qa.z, qa.w), acc[t]);
+            acc[t] = ptx::f2_fma(ptx::f2(kf[4], kf[5]), ptx::f2(qb.x, qb.y), acc[t]);
+            acc[t] = ptx::f2_fma(ptx::f2(kf[6], kf[7]), ptx::f2(qb.z, qb.w), acc[t]);
           }
         }
         // ---- online softmax per query over this warp's 32 keys
@@ -211,7 +207,9 @@ __device__ void dec_compute(const DecParams& p, uint8_t* base, uint32_t bars, co
 #pragma unroll
         for (int t = 0; t < SQ; ++t) {
           const bool vis = key <= last0 + t && key < w.L;
-          const float sv = vis ? s0[t] + s1[t] : -INFINITY;
+          float s0, s1;
+          ptx::f2_split(acc[t], s0, s1);
+          const float sv = vis ? s0 + s1 : -INFINITY;
           const float m_new = fmaxf(m[t], warp_max(sv));
           const float m_use = m_new == -INFINITY ? 0.0f : m_new;
           const float alpha = ptx::ex2(m[t] - m_use);
@@ -219,7 +217,12 @@ __device__ void dec_compute(const DecParams& p, uint8_t* base, uint32_t bars, co
           l[t] = l[t] * alpha + warp_sum(pr[t]);
           m[t] = m_new;
 #pragma unroll
-          for (int i = 0; i < DPL; ++i) o[t][i] *= alpha;
+          for (int i = 0; i < DPL; i += 2) {
+            float a0, a1;
+            ptx::f2_split(ptx::f2_mul(ptx::f2(o[t][i], o[t][i + 1]), ptx::f2(alpha, alpha)), a0, a1);
+            o[t][i] = a0;
+            o[t][i + 1] = a1;
+          }
         }
         // ---- O_t += p_t V over the 32 keys; lane owns DPL output dims
 #pragma unroll 4
@@ -242,7 +245,13 @@ __device__ void dec_compute(const DecParams& p, uint8_t* base, uint32_t bars, co
           for (int t = 0; t < SQ; ++t) {
             const float pv = __shfl_sync(0xffffffffu, pr[t], kk);
 #pragma unroll
-            for (int i = 0; i < DPL; ++i) o[t][i] = fmaf(pv, vf[i], o[t][i]);
+            for (int i = 0; i < DPL; i += 2) {
+              float a0, a1;
+              ptx::f2_split(ptx::f2_fma(ptx::f2(pv, pv), ptx::f2(vf[i], vf[i + 1]),
+                                        ptx::f2(o[t][i], o[t][i + 1])), a0, a1);
+              o[t][i] = a0;
+              o[t][i + 1] = a1;
+            }
           }
         }
       }
